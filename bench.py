@@ -1,0 +1,491 @@
+#!/usr/bin/env python
+"""Benchmark of the Q8_0 decode path on GB300.
+
+Headline workload: the decode feed-forward block of a 0.8B-shaped model (hidden
+1024, stacked gate|up 7168 x 1024, down 1024 x 3584, Q8_0 weights), batch 1.
+One step = one decode step's worth of that block: L chained layers (default 24)
+with distinct weights, replayed as one CUDA graph (RMSNorm+quantize, gate|up
+GEMV with SiLU*u, quantize, down GEMV with the residual folded in: 4 launches per
+layer).  The weights of one step (L x 11.7 MB) exceed the L2 cache, so every step
+streams them from HBM.
+
+Metric: achieved HBM GB/s = algorithmic bytes of the step / step time.  The line
+also carries the roofline of the dominant kernel (the gate|up GEMV), an
+end-to-end number through host buffers, the CPU oracle timed on the host, the SM
+clocks sampled during the timed region, and (unless --quick) the other
+workloads' kernel rates: Q8_0 GEMV 256x1024, bf16 projection 18432x2560,
+output-head GEMV 262144x1024 at batch 1/2/4/8, and the M=512 prompt contraction.
+
+--impl reference times the CPU oracle (the only reference this method has) on
+the same workload and prints the same line with "impl": "reference".
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Q8_0 decode GEMV achieved HBM GB/s (% of GB300 peak); prefill int8 TOPS"
+HIDDEN, FFN = 1024, 3584
+EPS = 1e-6
+# algorithmic bytes of one FFN layer: both weights (values + binary16 scales),
+# the input row x (f32), the RMSNorm gain (f32) and the output row (f32)
+W_GU_BYTES = 2 * FFN * HIDDEN + 2 * FFN * (HIDDEN // 32) * 2
+W_DN_BYTES = HIDDEN * FFN + HIDDEN * (FFN // 32) * 2
+LAYER_BYTES = W_GU_BYTES + W_DN_BYTES + 3 * HIDDEN * 4
+# gate|up GEMV per launch: weights, Q8_0 input (values + scales), h out (f32)
+GU_KERNEL_BYTES = W_GU_BYTES + HIDDEN + (HIDDEN // 32) * 2 + FFN * 4
+
+
+def workload_name(layers: int) -> str:
+    return (f"decode FFN, 0.8B-shaped (hidden {HIDDEN}, stacked gate|up {2 * FFN}x{HIDDEN}, down {HIDDEN}x{FFN}, "
+            f"Q8_0), batch 1, {layers} chained layers with distinct weights per step")
+
+
+def peaks():
+    p = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+    f = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(f):
+        m = json.load(open(f))
+        for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+            if k in m:
+                p[k] = float(m[k])
+        p["source"] = "measured"
+    return p
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region (NVML read-only queries)
+# --------------------------------------------------------------------------
+REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+           0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+           0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    """Polls the SM clock and the clock-event reasons of this process's GPU."""
+
+    def __init__(self, torch, dev: int):
+        self.ok = False
+        self.samples = []
+        self.reasons = 0
+        self.max_mhz = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            pr = torch.cuda.get_device_properties(dev)
+            bus = f"{getattr(pr, 'pci_domain_id', 0):08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0".encode()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) != 0:
+                if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(dev), ctypes.byref(h)) != 0:
+                    return
+            self.nv, self.h = nv, h
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._reason_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.ok = True
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def _read(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk)) == 0:
+            self.samples.append(clk.value)
+        if self._reason_fn(self.h, ctypes.byref(rs)) == 0:
+            self.reasons |= rs.value
+
+    def start(self):
+        self.samples, self.reasons = [], 0
+        self._stop = threading.Event()
+        if not self.ok:
+            return
+        self._read()
+
+        def loop():
+            while not self._stop.wait(0.002):
+                self._read()
+
+        self._t = threading.Thread(target=loop, daemon=True)
+        self._t.start()
+
+    def stop(self):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"], "samples": 0}
+        self._stop.set()
+        self._t.join()
+        self._read()
+        names = [n for b, n in REASONS.items() if self.reasons & b and b != 0x1]
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
+                "reasons": names, "samples": len(self.samples)}
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; no collective on the data path)
+# --------------------------------------------------------------------------
+class Dist:
+    def __init__(self, torch):
+        self.torch = torch
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+
+            torch.cuda.set_device(self.local)
+            dist.init_process_group("nccl")
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if not self.pg:
+            return v
+        t = self.torch.tensor([v], dtype=self.torch.float64, device="cuda")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# --------------------------------------------------------------------------
+# the workload on the GPU
+# --------------------------------------------------------------------------
+def make_layers(torch, n_layers: int, seed: int = 0):
+    from block_quantized_decode_rmsnorm_gb300 import api, synth
+
+    layers = []
+    for l in range(n_layers):
+        c = synth.ffn_case(seed, HIDDEN, FFN, layer=l)
+        layers.append(api.FFNLayer(torch.from_numpy(c["gamma"]).cuda(),
+                                   api.q8_weight_from_numpy(c["gu_qs"], c["gu_d"]),
+                                   api.q8_weight_from_numpy(c["dn_qs"], c["dn_d"])))
+        if l == 0:
+            x0 = c["x"]
+    return layers, x0
+
+
+def capture(torch, fn):
+    """Record fn() (which launches on the current stream) into a CUDA graph."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()  # warm the launch paths outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(torch, g, iters: int) -> float:
+    """Seconds per replay, CUDA events on the replay stream."""
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / iters
+
+
+def l2_copies(torch, bytes_one: int) -> int:
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    return max(2, -(-4 * l2 // bytes_one))
+
+
+def replicate_q8(torch, api, w0, copies: int):
+    """`copies` distinct device copies of a packed weight, carved from one allocation."""
+    qs = torch.empty((copies,) + tuple(w0.qs.shape), dtype=w0.qs.dtype, device="cuda")
+    d = torch.empty((copies,) + tuple(w0.d.shape), dtype=w0.d.dtype, device="cuda")
+    qs.copy_(w0.qs.unsqueeze(0).expand_as(qs))
+    d.copy_(w0.d.unsqueeze(0).expand_as(d))
+    return [api.Q8Weight(qs[i], d[i]) for i in range(copies)]
+
+
+def extra_configs(torch, pk) -> dict:
+    """Kernel rates on the other workloads, each cold (rotating copies >= 4x L2)."""
+    import numpy as np
+
+    from block_quantized_decode_rmsnorm_gb300 import api, synth
+
+    out = {}
+    hbm = pk["hbm_gbs"]
+
+    def gemv_rate(name, n, k, batch):
+        qs, d = synth.q8_0_weight_planes(0, synth.S_W0, n, k)
+        w0 = api.q8_weight_from_numpy(qs, d)
+        wbytes = w0.nbytes
+        copies = l2_copies(torch, wbytes)
+        ws = replicate_q8(torch, api, w0, copies)
+        x = torch.from_numpy(synth.f32_normal(0, synth.S_X, (batch, k))).cuda()
+        xq, xd = api.quantize_act_q8_0(x)
+        y = torch.empty((batch, n), dtype=torch.float32, device="cuda")
+        g = capture(torch, lambda: [api.qgemv_q8_0(w, xq, xd, y=y) for w in ws])
+        t = time_graph(torch, g, 5) / copies
+        algo = wbytes + batch * (k + (k // 32) * 2) + batch * n * 4
+        gbs = algo / t / 1e9
+        out[name] = {"us": t * 1e6, "GB/s": gbs, "frac_hbm": gbs / hbm, "bytes": algo, "copies": copies}
+        del ws, g
+
+    gemv_rate("q8_0_gemv_256x1024_b1", 256, 1024, 1)
+    for b in (1, 2, 4, 8):
+        gemv_rate(f"output_head_262144x1024_b{b}", 262144, 1024, b)
+
+    # bf16 projection with the norm fused in front, SiLU*u behind
+    bc = synth.bf16_case(0)
+    w0 = api.bf16_from_bits(bc["w"])
+    copies = l2_copies(torch, w0.numel() * 2)
+    ws = [w0] + [w0.clone() for _ in range(copies - 1)]
+    xb, gb = api.bf16_from_bits(bc["x"]), api.bf16_from_bits(bc["gamma"])
+    yb = torch.empty((w0.shape[0] // 2,), dtype=torch.float32, device="cuda")
+    g = capture(torch, lambda: [api.qgemv_bf16(w, xb, gb, EPS, epilogue="silu_mul", y=yb) for w in ws])
+    t = time_graph(torch, g, 5) / copies
+    algo = w0.numel() * 2 + 2 * 2 * w0.shape[1] + yb.numel() * 4
+    out["bf16_proj_18432x2560_norm_silu"] = {"us": t * 1e6, "GB/s": algo / t / 1e9,
+                                             "frac_hbm": algo / t / 1e9 / hbm, "bytes": algo, "copies": copies}
+    del ws, g
+
+    # prompt-sized contraction
+    pc = synth.prefill_case(0)
+    wp = api.q8_weight_from_numpy(pc["w_qs"], pc["w_d"])
+    copies = l2_copies(torch, wp.nbytes)
+    wps = replicate_q8(torch, api, wp, copies)
+    xq, xd = api.quantize_act_q8_0(torch.from_numpy(pc["x"]).cuda())
+    yp = torch.empty((512, 7168), dtype=torch.float32, device="cuda")
+    g = capture(torch, lambda: [api.qgemm_q8_0_prefill(w, xq, xd, y=yp) for w in wps])
+    t = time_graph(torch, g, 5) / copies
+    ops = 2 * 512 * 7168 * 1024
+    tops = ops / t / 1e12
+    out["prefill_512x7168x1024"] = {"us": t * 1e6, "TOPS": tops, "frac_bf16_dense_peak": tops / pk["bf16_tflops"],
+                                    "int_ops": ops, "path": "mma.sync m16n8k32 s8", "copies": copies}
+    del wps, g
+    torch.cuda.empty_cache()
+    _ = np
+    return out
+
+
+def ncu_traffic(kernel_key: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, or None when the kernel source changed since it was captured."""
+    f = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(f):
+        return None
+    rec = json.load(open(f)).get(kernel_key)
+    if not rec:
+        return None
+    if rec.get("source_sha256") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("qg_gemv.cu", "qg_common.cuh"):
+        with open(os.path.join(ROOT, "block_quantized_decode_rmsnorm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def cpu_baseline(seconds: float, n_layers: int) -> dict:
+    """The oracle, as it stands, on this host: FFN layers of the step until the
+    time budget is spent (one host thread)."""
+    import oracle
+    from block_quantized_decode_rmsnorm_gb300 import synth
+
+    oracle.build()
+    cases = [synth.ffn_case(0, HIDDEN, FFN, layer=l) for l in range(min(n_layers, 4))]
+    x = cases[0]["x"].copy()
+    done, t0 = 0, time.perf_counter()
+    while True:
+        c = cases[done % len(cases)]
+        r = oracle.decode_ffn(x, c["gamma"], EPS, c["gu_qs"], c["gu_d"], c["dn_qs"], c["dn_d"])
+        x = r["out"]
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": done * LAYER_BYTES / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} FFN layers (hidden {HIDDEN}, ffn {FFN}) of the {n_layers}-layer step in {el:.1f} s, "
+                      "plain C oracle, one host thread"}
+
+
+def run_ours(args):
+    import torch
+
+    from block_quantized_decode_rmsnorm_gb300 import api, build
+
+    dist = Dist(torch)
+    dev = dist.local if dist.world > 1 else 0
+    torch.cuda.set_device(dev)
+    build()
+    pk = peaks()
+    L = args.layers
+    layers, x0_np = make_layers(torch, L)
+    buf = api.FFNBuffers.allocate(HIDDEN, FFN, "cuda")
+    x = torch.from_numpy(x0_np).cuda()
+
+    def step():
+        for layer in layers:
+            api.decode_ffn_q8_0(x, layer, buf, EPS)
+
+    g = capture(torch, step)
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(torch, dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    e0.record()
+    for _ in range(args.steps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    dist.barrier()
+    elapsed = dist.max(e0.elapsed_time(e1) / 1e3)
+    step_bytes = L * LAYER_BYTES
+    value = dist.world * args.steps * step_bytes / elapsed / 1e9
+
+    # dominant kernel: the gate|up GEMV, launched back to back over the L layers
+    gu_graph = capture(torch, lambda: [api.qgemv_q8_0(l.gate_up, buf.xq, buf.xd, epilogue="silu_mul", y=buf.h)
+                                       for l in layers])
+    t_gu = time_graph(torch, gu_graph, max(5, args.steps // 4)) / L
+    achieved = GU_KERNEL_BYTES / t_gu / 1e9
+    roofline = {"bound": "hbm", "kernel": "gemv_q8_0_reg_kernel<1,1,2> (gate|up 7168x1024, SiLU*u)",
+                "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                "peak_source": pk["source"], "algorithmic_bytes_per_launch": GU_KERNEL_BYTES,
+                "launch_us": t_gu * 1e6, "traffic": ncu_traffic("gemv_q8_0_gate_up")}
+    del gu_graph
+
+    # end to end through host buffers: H2D of x, the step, D2H of the result, every step
+    x_host = torch.from_numpy(x0_np.copy()).pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+    for _ in range(max(3, args.warmup)):
+        x.copy_(x_host, non_blocking=True)
+        g.replay()
+        out_host.copy_(x, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        x.copy_(x_host, non_blocking=True)
+        g.replay()
+        out_host.copy_(x, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    e2e_el = dist.max(time.perf_counter() - t0)
+    e2e = {"value": dist.world * args.steps * step_bytes / e2e_el / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": HIDDEN * 4, "d2h_bytes_per_step": HIDDEN * 4,
+           "ms_per_step": e2e_el / args.steps * 1e3}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": dist.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": {"workload": workload_name(L), "layers": L, "batch": 1, "bytes_per_step": step_bytes,
+                   "frac_of_hbm_peak": value / dist.world / pk["hbm_gbs"],
+                   "l2": f"inputs larger than L2: {step_bytes / 1e6:.0f} MB of weights per step, "
+                         f"L2 {torch.cuda.get_device_properties(dev).L2_cache_size / 1e6:.0f} MB",
+                   "graph": f"one CUDA graph per step, {4 * L} launches, programmatic dependent launch",
+                   "parallelism": f"replicas x{dist.world} (independent decode streams, no collective)"},
+        "roofline": roofline, "e2e": e2e, "gpu_launches": 4 * L * args.steps, "clocks": clocks,
+    }
+    if not args.quick:
+        line["other_workloads"] = extra_configs(torch, pk)
+    if dist.rank == 0 and dist.world == 1:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds, L)
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: same workload, metric and unit."""
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    import oracle
+    from block_quantized_decode_rmsnorm_gb300 import synth
+
+    oracle.build()
+    L = args.layers
+    cases = [synth.ffn_case(0, HIDDEN, FFN, layer=l) for l in range(min(L, 4))]
+    x = cases[0]["x"].copy()
+    # one layer's time, then layers per step sized so the whole run ends in ~2 minutes
+    t0 = time.perf_counter()
+    oracle.decode_ffn(x, cases[0]["gamma"], EPS, cases[0]["gu_qs"], cases[0]["gu_d"], cases[0]["dn_qs"],
+                      cases[0]["dn_d"])
+    t_layer = max(time.perf_counter() - t0, 1e-4)
+    per_step = max(1, min(L, int(120.0 / ((args.steps + args.warmup) * t_layer))))
+
+    def step():
+        nonlocal x
+        for l in range(per_step):
+            c = cases[l % len(cases)]
+            x = oracle.decode_ffn(x, c["gamma"], EPS, c["gu_qs"], c["gu_d"], c["dn_qs"], c["dn_d"])["out"]
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = args.steps * per_step * LAYER_BYTES / el / 1e9
+    sample = (f"{per_step} of the {L} FFN layers per step (hidden {HIDDEN}, ffn {FFN}), plain C oracle, "
+              "one host thread")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_name(L), "layers": L, "batch": 1, "layers_per_step_sampled": per_step},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=24)
+    ap.add_argument("--quick", action="store_true", help="skip the other workloads' kernel rates")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

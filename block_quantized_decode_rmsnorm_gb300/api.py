@@ -1,0 +1,281 @@
+"""Torch-tensor front end of libqgemv.so: argument marshalling only.
+
+Each function has the name of the C entry point it calls (include/qgemv.h),
+checks dtypes, shapes and devices, allocates outputs that were not given (torch
+owns all device memory), and passes raw pointers and the current CUDA stream.
+All arithmetic happens in the library's kernels.
+
+Tensor formats
+--------------
+* Q8_0 values: ``torch.int8 [rows, k]``; Q8_0 scales: ``torch.float16
+  [rows, k/32]`` (the library reads the binary16 bit patterns).
+* Weights in the packed layout: a ``Q8Weight(qs, d)`` pair as above.
+* bf16 tensors: ``torch.bfloat16``.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+from ._lib import QG_EPI_NONE, QG_EPI_RESIDUAL_ADD, QG_EPI_SILU_MUL_HALVES  # noqa: F401
+
+EPILOGUES = {"none": QG_EPI_NONE, "silu_mul": QG_EPI_SILU_MUL_HALVES, "residual": QG_EPI_RESIDUAL_ADD}
+
+
+@dataclass
+class Q8Weight:
+    """Packed Q8_0 weight: values int8 [n_rows, k] and binary16 scales [n_rows, k/32]."""
+
+    qs: torch.Tensor
+    d: torch.Tensor
+
+    @property
+    def n_rows(self) -> int:
+        return self.qs.shape[0]
+
+    @property
+    def k(self) -> int:
+        return self.qs.shape[1]
+
+    @property
+    def nbytes(self) -> int:
+        return self.qs.numel() + 2 * self.d.numel()
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if hasattr(stream, "cuda_stream"):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape=None) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device (there is no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _as_2d(x: torch.Tensor) -> torch.Tensor:
+    return x.unsqueeze(0) if x.dim() == 1 else x
+
+
+# --------------------------------------------------------------------------
+# entry points
+# --------------------------------------------------------------------------
+
+def qg_q8_0_pack(blocks: torch.Tensor, n_rows: int, k: int, out: Q8Weight | None = None, stream=None) -> Q8Weight:
+    """Canonical 34-byte Q8_0 blocks (uint8, n_rows*(k/32)*34 bytes) -> packed planes."""
+    _need(blocks, "blocks", torch.uint8)
+    if blocks.numel() != n_rows * (k // 32) * 34:
+        raise ValueError("blocks has the wrong number of bytes for n_rows, k")
+    dev = blocks.device
+    if out is None:
+        out = Q8Weight(torch.empty((n_rows, k), dtype=torch.int8, device=dev),
+                       torch.empty((n_rows, k // 32), dtype=torch.float16, device=dev))
+    _need(out.qs, "out.qs", torch.int8, (n_rows, k))
+    _need(out.d, "out.d", torch.float16, (n_rows, k // 32))
+    _lib.call("qg_q8_0_pack", blocks.data_ptr(), n_rows, k, out.qs.data_ptr(), out.d.data_ptr(),
+              _stream_handle(stream))
+    return out
+
+
+def quantize_act_q8_0(x: torch.Tensor, q: torch.Tensor | None = None, d: torch.Tensor | None = None, stream=None):
+    """f32 [rows, k] (or [k]) -> (q int8 [rows, k], d float16 [rows, k/32])."""
+    _need(x, "x", torch.float32)
+    x2 = _as_2d(x)
+    rows, k = x2.shape
+    if q is None:
+        q = torch.empty((rows, k), dtype=torch.int8, device=x.device)
+    if d is None:
+        d = torch.empty((rows, k // 32), dtype=torch.float16, device=x.device)
+    _need(q, "q", torch.int8, (rows, k))
+    _need(d, "d", torch.float16, (rows, k // 32))
+    _lib.call("quantize_act_q8_0", x2.data_ptr(), rows, k, q.data_ptr(), d.data_ptr(), _stream_handle(stream))
+    return q, d
+
+
+def rmsnorm_quantize(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6, q=None, d=None, inv_rms=None,
+                     stream=None):
+    """RMSNorm(x) * gamma quantized to Q8_0; returns (q, d, inv_rms)."""
+    _need(x, "x", torch.float32)
+    x2 = _as_2d(x)
+    rows, k = x2.shape
+    _need(gamma, "gamma", torch.float32, (k,))
+    if q is None:
+        q = torch.empty((rows, k), dtype=torch.int8, device=x.device)
+    if d is None:
+        d = torch.empty((rows, k // 32), dtype=torch.float16, device=x.device)
+    if inv_rms is None:
+        inv_rms = torch.empty((rows,), dtype=torch.float32, device=x.device)
+    _need(q, "q", torch.int8, (rows, k))
+    _need(d, "d", torch.float16, (rows, k // 32))
+    _need(inv_rms, "inv_rms", torch.float32, (rows,))
+    _lib.call("rmsnorm_quantize", x2.data_ptr(), gamma.data_ptr(), rows, k, float(eps), q.data_ptr(), d.data_ptr(),
+              inv_rms.data_ptr(), _stream_handle(stream))
+    return q, d, inv_rms
+
+
+def qgemv_q8_0(w: Q8Weight, xq: torch.Tensor, xd: torch.Tensor, epilogue: str | int = "none",
+               residual: torch.Tensor | None = None, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Block-scaled Q8_0 GEMV; y f32 [batch, n_out]."""
+    epi = EPILOGUES[epilogue] if isinstance(epilogue, str) else int(epilogue)
+    _need(w.qs, "w.qs", torch.int8)
+    n_rows, k = w.qs.shape
+    _need(w.d, "w.d", torch.float16, (n_rows, k // 32))
+    xq2, xd2 = _as_2d(xq), _as_2d(xd)
+    batch = xq2.shape[0]
+    _need(xq2, "xq", torch.int8, (batch, k))
+    _need(xd2, "xd", torch.float16, (batch, k // 32))
+    n_out = n_rows // 2 if epi == QG_EPI_SILU_MUL_HALVES else n_rows
+    if y is None:
+        y = torch.empty((batch, n_out), dtype=torch.float32, device=w.qs.device)
+    _need(_as_2d(y), "y", torch.float32, (batch, n_out))
+    if residual is not None:
+        _need(_as_2d(residual), "residual", torch.float32, (batch, n_rows))
+    _lib.call("qgemv_q8_0", w.qs.data_ptr(), w.d.data_ptr(), n_rows, k, xq2.data_ptr(), xd2.data_ptr(), batch, epi,
+              _ptr(residual), y.data_ptr(), _stream_handle(stream))
+    return y
+
+
+def qgemv_bf16(w: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor | None = None, eps: float = 1e-6,
+               epilogue: str | int = "none", residual: torch.Tensor | None = None, y: torch.Tensor | None = None,
+               stream=None) -> torch.Tensor:
+    """bf16 GEMV with optional fused RMSNorm in front; y f32 [n_out]."""
+    epi = EPILOGUES[epilogue] if isinstance(epilogue, str) else int(epilogue)
+    _need(w, "w", torch.bfloat16)
+    n_rows, k = w.shape
+    _need(x, "x", torch.bfloat16, (k,))
+    if gamma is not None:
+        _need(gamma, "gamma", torch.bfloat16, (k,))
+    n_out = n_rows // 2 if epi == QG_EPI_SILU_MUL_HALVES else n_rows
+    if y is None:
+        y = torch.empty((n_out,), dtype=torch.float32, device=w.device)
+    _need(y, "y", torch.float32, (n_out,))
+    if residual is not None:
+        _need(residual, "residual", torch.float32, (n_rows,))
+    _lib.call("qgemv_bf16", w.data_ptr(), n_rows, k, x.data_ptr(), _ptr(gamma), float(eps), epi, _ptr(residual),
+              y.data_ptr(), _stream_handle(stream))
+    return y
+
+
+def qgemm_q8_0_prefill(w: Q8Weight, xq: torch.Tensor, xd: torch.Tensor, y: torch.Tensor | None = None,
+                       stream=None) -> torch.Tensor:
+    """Prompt-sized block-scaled contraction; Y f32 [m, n_rows]."""
+    _need(w.qs, "w.qs", torch.int8)
+    n_rows, k = w.qs.shape
+    _need(w.d, "w.d", torch.float16, (n_rows, k // 32))
+    m = xq.shape[0]
+    _need(xq, "xq", torch.int8, (m, k))
+    _need(xd, "xd", torch.float16, (m, k // 32))
+    if y is None:
+        y = torch.empty((m, n_rows), dtype=torch.float32, device=w.qs.device)
+    _need(y, "y", torch.float32, (m, n_rows))
+    _lib.call("qgemm_q8_0_prefill", w.qs.data_ptr(), w.d.data_ptr(), n_rows, k, xq.data_ptr(), xd.data_ptr(), m,
+              y.data_ptr(), _stream_handle(stream))
+    return y
+
+
+def qg_debug_block_dots_q8_0(w: Q8Weight, xq: torch.Tensor, s: torch.Tensor | None = None,
+                             stream=None) -> torch.Tensor:
+    """Exact int32 block sums s[batch, n_rows, k/32]."""
+    n_rows, k = w.qs.shape
+    xq2 = _as_2d(xq)
+    batch = xq2.shape[0]
+    _need(xq2, "xq", torch.int8, (batch, k))
+    if s is None:
+        s = torch.empty((batch, n_rows, k // 32), dtype=torch.int32, device=w.qs.device)
+    _need(s, "s", torch.int32, (batch, n_rows, k // 32))
+    _lib.call("qg_debug_block_dots_q8_0", w.qs.data_ptr(), n_rows, k, xq2.data_ptr(), batch, s.data_ptr(),
+              _stream_handle(stream))
+    return s
+
+
+# --------------------------------------------------------------------------
+# composite: one decode FFN step (four launches, graph-capturable)
+# --------------------------------------------------------------------------
+
+@dataclass
+class FFNLayer:
+    """Weights of one decode feed-forward block: RMSNorm gain, stacked gate|up, down."""
+
+    gamma: torch.Tensor  # f32 [hidden]
+    gate_up: Q8Weight    # [2*ffn, hidden]
+    down: Q8Weight       # [hidden, ffn]
+
+    @property
+    def nbytes(self) -> int:
+        return self.gate_up.nbytes + self.down.nbytes
+
+
+@dataclass
+class FFNBuffers:
+    """Stable activation buffers reused by every step (graph replay needs fixed addresses)."""
+
+    xq: torch.Tensor
+    xd: torch.Tensor
+    h: torch.Tensor
+    hq: torch.Tensor
+    hd: torch.Tensor
+
+    @staticmethod
+    def allocate(hidden: int, ffn: int, device) -> "FFNBuffers":
+        return FFNBuffers(
+            torch.empty((1, hidden), dtype=torch.int8, device=device),
+            torch.empty((1, hidden // 32), dtype=torch.float16, device=device),
+            torch.empty((1, ffn), dtype=torch.float32, device=device),
+            torch.empty((1, ffn), dtype=torch.int8, device=device),
+            torch.empty((1, ffn // 32), dtype=torch.float16, device=device),
+        )
+
+
+def decode_ffn_q8_0(x: torch.Tensor, layer: FFNLayer, buf: FFNBuffers, eps: float = 1e-6, stream=None) -> None:
+    """x <- x + down(SiLU(gate(n)) * up(n)), n = Q8_0(RMSNorm(x) * gamma), in place.
+
+    "Filling in the blanks: Inference using Phobos", Fast Decode: the activation
+    is quantized once and shared, the projections reading it are stacked, and the
+    residual add is folded into the last matmul.
+    """
+    s = _stream_handle(stream)
+    hidden = x.shape[-1]
+    ffn = layer.down.k
+    _lib.call("rmsnorm_quantize", x.data_ptr(), layer.gamma.data_ptr(), 1, hidden, float(eps), buf.xq.data_ptr(),
+              buf.xd.data_ptr(), None, s)
+    _lib.call("qgemv_q8_0", layer.gate_up.qs.data_ptr(), layer.gate_up.d.data_ptr(), 2 * ffn, hidden,
+              buf.xq.data_ptr(), buf.xd.data_ptr(), 1, QG_EPI_SILU_MUL_HALVES, None, buf.h.data_ptr(), s)
+    _lib.call("quantize_act_q8_0", buf.h.data_ptr(), 1, ffn, buf.hq.data_ptr(), buf.hd.data_ptr(), s)
+    _lib.call("qgemv_q8_0", layer.down.qs.data_ptr(), layer.down.d.data_ptr(), hidden, ffn, buf.hq.data_ptr(),
+              buf.hd.data_ptr(), 1, QG_EPI_RESIDUAL_ADD, x.data_ptr(), x.data_ptr(), s)
+
+
+# --------------------------------------------------------------------------
+# host <-> device helpers (plumbing)
+# --------------------------------------------------------------------------
+
+def q8_weight_from_numpy(qs, d, device="cuda") -> Q8Weight:
+    """Upload numpy planes (int8 values, uint16 binary16 bits) as a packed weight."""
+    import numpy as np
+
+    qs_t = torch.from_numpy(np.ascontiguousarray(qs, dtype=np.int8)).to(device)
+    d_t = torch.from_numpy(np.ascontiguousarray(d, dtype=np.uint16).view(np.float16)).to(device)
+    return Q8Weight(qs_t, d_t)
+
+
+def bf16_from_bits(bits, device="cuda") -> torch.Tensor:
+    import numpy as np
+
+    return torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint16).view(np.int16)).to(device).view(torch.bfloat16)

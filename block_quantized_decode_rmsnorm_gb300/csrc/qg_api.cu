@@ -1,0 +1,173 @@
+// extern "C" entry points of libqgemv.so: argument checks, then one launch.
+// Declarations and the full contract are in include/qgemv.h.
+#include <mutex>
+
+#include "qg_common.cuh"
+
+namespace qg {
+
+cudaError_t launch_quantize_act(const float *, int64_t, int64_t, int8_t *, uint16_t *, cudaStream_t);
+cudaError_t launch_rmsnorm_quantize(const float *, const float *, int64_t, int64_t, float, int8_t *, uint16_t *,
+                                    float *, cudaStream_t);
+cudaError_t launch_pack_q8_0(const void *, int64_t, int64_t, int8_t *, uint16_t *, cudaStream_t);
+cudaError_t launch_gemv_q8_0(const int8_t *, const uint16_t *, int64_t, int64_t, const int8_t *, const uint16_t *,
+                             int64_t, int, const float *, float *, cudaStream_t);
+cudaError_t launch_block_dots(const int8_t *, int64_t, int64_t, const int8_t *, int64_t, int32_t *, cudaStream_t);
+cudaError_t launch_gemv_bf16(const uint16_t *, int64_t, int64_t, const uint16_t *, const uint16_t *, float, int,
+                             const float *, float *, cudaStream_t);
+cudaError_t launch_prefill_mma(const int8_t *, const uint16_t *, int64_t, int64_t, const int8_t *, const uint16_t *,
+                               int64_t, float *, cudaStream_t);
+
+// SM count of the current device, read once per device.
+int num_sms()
+{
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+}  // namespace qg
+
+namespace {
+
+constexpr int64_t kMaxK = int64_t(1) << 20;       // longest supported reduction
+constexpr int64_t kMaxRows = int64_t(1) << 31;    // rows per call
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+qg_status from_cuda(cudaError_t e)
+{
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return e == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
+qg_status check_q8_k(int64_t k)
+{
+    if (k <= 0 || k % 32 != 0 || k > kMaxK) return QG_ERR_SHAPE;
+    return QG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *qg_status_str(qg_status s)
+{
+    switch (s) {
+    case QG_OK: return "ok";
+    case QG_ERR_NULL: return "null pointer";
+    case QG_ERR_ALIGN: return "misaligned pointer";
+    case QG_ERR_SHAPE: return "bad shape";
+    case QG_ERR_UNSUPPORTED: return "unsupported request";
+    case QG_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+int qg_abi_version(void) { return 1; }
+
+qg_status qg_q8_0_pack(const void *blocks, int64_t n_rows, int64_t k, int8_t *qs, uint16_t *d, qg_stream_t stream)
+{
+    if (n_rows < 0 || n_rows > kMaxRows) return QG_ERR_SHAPE;
+    if (qg_status st = check_q8_k(k); st != QG_OK) return st;
+    if (n_rows == 0) return QG_OK;
+    if (!blocks || !qs || !d) return QG_ERR_NULL;
+    if (!aligned(qs, 32) || !aligned(d, 2)) return QG_ERR_ALIGN;
+    return from_cuda(qg::launch_pack_q8_0(blocks, n_rows, k, qs, d, stream));
+}
+
+qg_status quantize_act_q8_0(const float *x, int64_t rows, int64_t k, int8_t *q, uint16_t *d, qg_stream_t stream)
+{
+    if (rows < 0 || rows > kMaxRows) return QG_ERR_SHAPE;
+    if (qg_status st = check_q8_k(k); st != QG_OK) return st;
+    if (rows == 0) return QG_OK;
+    if (!x || !q || !d) return QG_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(q, 16) || !aligned(d, 2)) return QG_ERR_ALIGN;
+    return from_cuda(qg::launch_quantize_act(x, rows, k, q, d, stream));
+}
+
+qg_status rmsnorm_quantize(const float *x, const float *gamma, int64_t rows, int64_t k, float eps, int8_t *q,
+                           uint16_t *d, float *inv_rms, qg_stream_t stream)
+{
+    if (rows < 0 || rows > (int64_t(1) << 31) - 1) return QG_ERR_SHAPE;
+    if (qg_status st = check_q8_k(k); st != QG_OK) return st;
+    if (k > 65536) return QG_ERR_SHAPE;
+    if (!(eps >= 0.0f)) return QG_ERR_SHAPE;
+    if (rows == 0) return QG_OK;
+    if (!x || !gamma || !q || !d) return QG_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(gamma, 16) || !aligned(q, 16) || !aligned(d, 2) || !aligned(inv_rms, 4))
+        return QG_ERR_ALIGN;
+    return from_cuda(qg::launch_rmsnorm_quantize(x, gamma, rows, k, eps, q, d, inv_rms, stream));
+}
+
+qg_status qgemv_q8_0(const int8_t *w_qs, const uint16_t *w_d, int64_t n_rows, int64_t k, const int8_t *xq,
+                     const uint16_t *xd, int64_t batch, int epilogue, const float *residual, float *y,
+                     qg_stream_t stream)
+{
+    if (n_rows < 0 || n_rows > kMaxRows) return QG_ERR_SHAPE;
+    if (qg_status st = check_q8_k(k); st != QG_OK) return st;
+    if (batch < 1) return QG_ERR_SHAPE;
+    if (batch > 8) return QG_ERR_UNSUPPORTED;
+    if (epilogue != QG_EPI_NONE && epilogue != QG_EPI_SILU_MUL_HALVES && epilogue != QG_EPI_RESIDUAL_ADD)
+        return QG_ERR_UNSUPPORTED;
+    if (epilogue == QG_EPI_SILU_MUL_HALVES && (n_rows % 2) != 0) return QG_ERR_SHAPE;
+    if (n_rows == 0) return QG_OK;
+    if (!w_qs || !w_d || !xq || !xd || !y) return QG_ERR_NULL;
+    if (epilogue == QG_EPI_RESIDUAL_ADD && !residual) return QG_ERR_NULL;
+    if (!aligned(w_qs, 32) || !aligned(w_d, 2) || !aligned(xq, 16) || !aligned(xd, 2) || !aligned(y, 16))
+        return QG_ERR_ALIGN;
+    if (epilogue == QG_EPI_RESIDUAL_ADD && !aligned(residual, 16)) return QG_ERR_ALIGN;
+    return from_cuda(qg::launch_gemv_q8_0(w_qs, w_d, n_rows, k, xq, xd, batch, epilogue, residual, y, stream));
+}
+
+qg_status qgemv_bf16(const uint16_t *w, int64_t n_rows, int64_t k, const uint16_t *x, const uint16_t *gamma,
+                     float eps, int epilogue, const float *residual, float *y, qg_stream_t stream)
+{
+    if (n_rows < 0 || n_rows > kMaxRows) return QG_ERR_SHAPE;
+    if (k <= 0 || k % 8 != 0 || k > 16384) return QG_ERR_SHAPE;
+    if (!(eps >= 0.0f)) return QG_ERR_SHAPE;
+    if (epilogue != QG_EPI_NONE && epilogue != QG_EPI_SILU_MUL_HALVES && epilogue != QG_EPI_RESIDUAL_ADD)
+        return QG_ERR_UNSUPPORTED;
+    if (epilogue == QG_EPI_SILU_MUL_HALVES && (n_rows % 2) != 0) return QG_ERR_SHAPE;
+    if (n_rows == 0) return QG_OK;
+    if (!w || !x || !y) return QG_ERR_NULL;
+    if (epilogue == QG_EPI_RESIDUAL_ADD && !residual) return QG_ERR_NULL;
+    if (!aligned(w, 16) || !aligned(x, 16) || !aligned(gamma, 16) || !aligned(y, 16)) return QG_ERR_ALIGN;
+    if (epilogue == QG_EPI_RESIDUAL_ADD && !aligned(residual, 16)) return QG_ERR_ALIGN;
+    return from_cuda(qg::launch_gemv_bf16(w, n_rows, k, x, gamma, eps, epilogue, residual, y, stream));
+}
+
+qg_status qgemm_q8_0_prefill(const int8_t *w_qs, const uint16_t *w_d, int64_t n_rows, int64_t k, const int8_t *xq,
+                             const uint16_t *xd, int64_t m, float *y, qg_stream_t stream)
+{
+    if (n_rows < 0 || n_rows > kMaxRows || m < 0 || m > (int64_t(1) << 24)) return QG_ERR_SHAPE;
+    if (qg_status st = check_q8_k(k); st != QG_OK) return st;
+    if (k > 8192) return QG_ERR_UNSUPPORTED;
+    if (n_rows == 0 || m == 0) return QG_OK;
+    if (!w_qs || !w_d || !xq || !xd || !y) return QG_ERR_NULL;
+    if (!aligned(w_qs, 32) || !aligned(w_d, 2) || !aligned(xq, 16) || !aligned(xd, 2) || !aligned(y, 16))
+        return QG_ERR_ALIGN;
+    return from_cuda(qg::launch_prefill_mma(w_qs, w_d, n_rows, k, xq, xd, m, y, stream));
+}
+
+qg_status qg_debug_block_dots_q8_0(const int8_t *w_qs, int64_t n_rows, int64_t k, const int8_t *xq, int64_t batch,
+                                   int32_t *s, qg_stream_t stream)
+{
+    if (n_rows < 0 || n_rows > kMaxRows) return QG_ERR_SHAPE;
+    if (qg_status st = check_q8_k(k); st != QG_OK) return st;
+    if (batch < 1 || batch > 8) return QG_ERR_SHAPE;
+    if (n_rows == 0) return QG_OK;
+    if (!w_qs || !xq || !s) return QG_ERR_NULL;
+    if (!aligned(w_qs, 32) || !aligned(xq, 16) || !aligned(s, 4)) return QG_ERR_ALIGN;
+    return from_cuda(qg::launch_block_dots(w_qs, n_rows, k, xq, batch, s, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,147 @@
+// Device helpers shared by the kernels of libqgemv.so (sm_103a only).
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/qgemv.h"
+
+#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ < 1000)
+#error "libqgemv targets Blackwell (sm_103a) only"
+#endif
+
+namespace qg {
+
+constexpr int QK = 32;  // values per Q8_0 block
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// stream serialization attribute may begin before its predecessor ends; it
+// must call pdl_wait() before it reads anything the predecessor writes or
+// writes anything the predecessor reads.  pdl_trigger() lets the successor
+// launch early.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// Loads
+// ---------------------------------------------------------------------------
+struct u32x8 {
+    uint32_t v[8];
+};
+
+// 32 bytes of streamed, read-only data (weights): one 256-bit load, not kept in
+// L1, with a 256-byte L2 prefetch hint.  p must be 32-byte aligned.
+__device__ __forceinline__ u32x8 ld_stream_32B(const void *p)
+{
+    u32x8 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3]), "=r"(r.v[4]), "=r"(r.v[5]),
+                   "=r"(r.v[6]), "=r"(r.v[7])
+                 : "l"(p));
+    return r;
+}
+
+// 16 bytes through the read-only path.  p must be 16-byte aligned.
+__device__ __forceinline__ uint4 ld_nc_16B(const void *p)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint16_t ld_nc_u16(const uint16_t *p)
+{
+    uint16_t r;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(r) : "l"(p));
+    return r;
+}
+
+// 16 bytes of data written by the previous kernel (coherent path, after pdl_wait).
+__device__ __forceinline__ uint4 ld_16B(const void *p) { return *reinterpret_cast<const uint4 *>(p); }
+
+// binary16 bits -> f32 (exact)
+__device__ __forceinline__ float h2f(uint16_t h) { return __half2float(__ushort_as_half(h)); }
+
+// f32 -> binary16 bits, round to nearest even
+__device__ __forceinline__ uint16_t f2h_rn(float f) { return __half_as_ushort(__float2half_rn(f)); }
+
+// 4-way int8 dot product accumulate (dp4a)
+__device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c)
+{
+    return __dp4a(static_cast<int>(a), static_cast<int>(b), c);
+}
+
+// Exact int32 -> f32 for |s| < 2^22 without the conversion pipe: place s in
+// the mantissa of 1.5 * 2^23 (integer add) and subtract that constant.
+__device__ __forceinline__ float small_int_to_float(int s)
+{
+    return __int_as_float(s + 0x4B400000) - 12582912.0f;
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ double warp_sum_f64(double v)
+{
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Q8_0 code of one value given the block's f32 scale d: round half away from
+// zero of v / d (IEEE division), clamped to [-127, 127]; 0 when d == 0.
+__device__ __forceinline__ int q8_code(float v, float d)
+{
+    if (d == 0.0f) return 0;
+    float t = roundf(__fdiv_rn(v, d));
+    t = fminf(fmaxf(t, -127.0f), 127.0f);
+    return static_cast<int>(t);
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u)
+{
+    return __fdiv_rn(g, 1.0f + expf(-g)) * u;
+}
+
+}  // namespace qg
+
+// ---------------------------------------------------------------------------
+// Host-side launch helpers (defined in qg_api.cu)
+// ---------------------------------------------------------------------------
+namespace qg {
+int num_sms();
+// Launch with programmatic stream serialization enabled.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+}  // namespace qg

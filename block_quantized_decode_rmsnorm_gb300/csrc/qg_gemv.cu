@@ -1,0 +1,357 @@
+// Q8_0 block-scaled matrix-vector product (decode) and the exact block-dot export.
+//
+// "Filling in the blanks: Inference using Phobos", Fast Decode: decode reads
+// every weight once (about 2 ops per byte, memory-bound); the dot products run
+// in int8 end to end (dp4a); a warp owns an output row and reduces with
+// shuffles; the residual add is folded into the matmul.  "One level down: #002
+// the same compiler on a GPU", Emitting for a GPU: gate and up are one stacked
+// projection with the activation fused behind it.
+//
+// GB300 mapping: lane j of a warp owns 32-value blocks j, j+32, ... of a row and
+// fetches each block's 32 int8 values with ONE 256-bit load, so a warp reads
+// 1 KB of a row per instruction, fully coalesced.  Each lane computes the exact
+// int32 block sum with eight dp4a and applies d_w*d_x once per block; the 32
+// lane partials are reduced with shuffles.  A warp handles R rows per task (R
+// independent 1 KB loads in flight per lane-iteration).  The first task's
+// weights are requested before the programmatic-dependent-launch wait, so the
+// weight stream overlaps the tail of the kernel that produces the activation.
+#include <mutex>
+#include <unordered_map>
+
+#include "qg_common.cuh"
+
+namespace qg {
+
+struct GemvParams {
+    const int8_t *w_qs;
+    const uint16_t *w_d;
+    const int8_t *xq;
+    const uint16_t *xd;
+    const float *residual;
+    float *y;
+    int64_t n_rows;
+    int64_t n_out;    // outputs per batch row
+    int64_t n_tasks;  // tasks of R weight rows
+    int64_t half;     // n_rows / 2 (stacked gate|up)
+    int k;
+    int nb;
+    int epi;
+    int batch;  // live batch rows (<= the compiled width B)
+};
+
+constexpr int GEMV_THREADS = 128;
+
+// Weight row of slot s in task t, or -1 past the end.  With the SiLU(g)*u
+// epilogue a task covers R/2 outputs, slot pairs (gate row o, up row o + F).
+template <int R>
+__device__ __forceinline__ int64_t slot_row(const GemvParams &p, int64_t t, int s)
+{
+    if (p.epi == QG_EPI_SILU_MUL_HALVES) {
+        const int64_t o = t * (R / 2) + (s >> 1);
+        return o < p.half ? o + (s & 1) * p.half : -1;
+    }
+    const int64_t r = t * R + s;
+    return r < p.n_rows ? r : -1;
+}
+
+// Reduce acc over the warp and write the R*B results of task t.  Lane
+// (s*B + b) writes slot s of batch row b.
+template <int B, int R>
+__device__ __forceinline__ void reduce_and_store(const GemvParams &p, int64_t t, int lane, float (&acc)[R][B])
+{
+    float val = 0.0f;
+#pragma unroll
+    for (int s = 0; s < R; ++s)
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+            const float v = warp_sum(acc[s][b]);
+            if (lane == s * B + b) val = v;
+        }
+    const int s = lane / B;
+    const int b = lane % B;
+    if (p.epi == QG_EPI_SILU_MUL_HALVES) {
+        const float u = __shfl_down_sync(0xffffffffu, val, B);  // slot s+1 = up row of the pair
+        if (lane < R * B && (s & 1) == 0 && b < p.batch) {
+            const int64_t o = t * (R / 2) + (s >> 1);
+            if (o < p.half) p.y[b * p.n_out + o] = silu_mul(val, u);
+        }
+        return;
+    }
+    if (lane < R * B && b < p.batch) {
+        const int64_t row = t * R + s;
+        if (row < p.n_rows) {
+            float out = val;
+            if (p.epi == QG_EPI_RESIDUAL_ADD) out = p.residual[b * p.n_rows + row] + val;
+            p.y[b * p.n_out + row] = out;
+        }
+    }
+}
+
+// Fast path: nb <= 32*NBL, activation (B rows x NBL blocks per lane) held in
+// registers for the whole kernel.
+template <int B, int NBL, int R>
+__global__ void __launch_bounds__(GEMV_THREADS) gemv_q8_0_reg_kernel(const GemvParams p)
+{
+    const int lane = threadIdx.x & 31;
+    const int wpc = blockDim.x >> 5;
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * wpc + (threadIdx.x >> 5);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * wpc;
+
+    u32x8 w[R][NBL];
+    float wd[R][NBL];
+
+#define QG_LOAD_WEIGHTS(T)                                                                   \
+    _Pragma("unroll") for (int s = 0; s < R; ++s)                                            \
+    {                                                                                        \
+        const int64_t row = slot_row<R>(p, (T), s);                                          \
+        _Pragma("unroll") for (int j = 0; j < NBL; ++j)                                      \
+        {                                                                                    \
+            const int blk = lane + 32 * j;                                                   \
+            if (row >= 0 && blk < p.nb) {                                                    \
+                w[s][j] = ld_stream_32B(p.w_qs + row * p.k + blk * QK);                      \
+                wd[s][j] = h2f(ld_nc_u16(p.w_d + row * p.nb + blk));                         \
+            } else {                                                                         \
+                _Pragma("unroll") for (int i = 0; i < 8; ++i) w[s][j].v[i] = 0u;             \
+                wd[s][j] = 0.0f;                                                             \
+            }                                                                                \
+        }                                                                                    \
+    }
+
+    if (t0 < p.n_tasks) { QG_LOAD_WEIGHTS(t0) }
+    pdl_trigger();
+    pdl_wait();
+
+    u32x8 xv[B][NBL];
+    float xs[B][NBL];
+#pragma unroll
+    for (int b = 0; b < B; ++b)
+#pragma unroll
+        for (int j = 0; j < NBL; ++j) {
+            const int blk = lane + 32 * j;
+            if (blk < p.nb && b < p.batch) {
+                const int8_t *src = p.xq + static_cast<int64_t>(b) * p.k + blk * QK;
+                const uint4 lo = ld_16B(src);
+                const uint4 hi = ld_16B(src + 16);
+                xv[b][j].v[0] = lo.x; xv[b][j].v[1] = lo.y; xv[b][j].v[2] = lo.z; xv[b][j].v[3] = lo.w;
+                xv[b][j].v[4] = hi.x; xv[b][j].v[5] = hi.y; xv[b][j].v[6] = hi.z; xv[b][j].v[7] = hi.w;
+                xs[b][j] = h2f(p.xd[static_cast<int64_t>(b) * p.nb + blk]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) xv[b][j].v[i] = 0u;
+                xs[b][j] = 0.0f;
+            }
+        }
+
+    for (int64_t t = t0; t < p.n_tasks; t += stride) {
+        float acc[R][B];
+#pragma unroll
+        for (int s = 0; s < R; ++s)
+#pragma unroll
+            for (int b = 0; b < B; ++b) acc[s][b] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NBL; ++j)
+#pragma unroll
+            for (int s = 0; s < R; ++s)
+#pragma unroll
+                for (int b = 0; b < B; ++b) {
+                    int S = 0;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) S = dp4a(w[s][j].v[i], xv[b][j].v[i], S);
+                    acc[s][b] = fmaf(small_int_to_float(S), wd[s][j] * xs[b][j], acc[s][b]);
+                }
+        const int64_t tn = t + stride;
+        if (tn < p.n_tasks) { QG_LOAD_WEIGHTS(tn) }  // in flight during the reduction below
+        reduce_and_store<B, R>(p, t, lane, acc);
+    }
+#undef QG_LOAD_WEIGHTS
+}
+
+// Generic path: any nb; activation read through L1 per block.
+template <int B, int R>
+__global__ void __launch_bounds__(GEMV_THREADS) gemv_q8_0_generic_kernel(const GemvParams p)
+{
+    const int lane = threadIdx.x & 31;
+    const int wpc = blockDim.x >> 5;
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * wpc + (threadIdx.x >> 5);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * wpc;
+    pdl_trigger();
+    pdl_wait();
+    for (int64_t t = t0; t < p.n_tasks; t += stride) {
+        float acc[R][B];
+#pragma unroll
+        for (int s = 0; s < R; ++s)
+#pragma unroll
+            for (int b = 0; b < B; ++b) acc[s][b] = 0.0f;
+        int64_t rows[R];
+#pragma unroll
+        for (int s = 0; s < R; ++s) rows[s] = slot_row<R>(p, t, s);
+        for (int j0 = 0; j0 < p.nb; j0 += 32) {
+            const int blk = j0 + lane;
+            if (blk >= p.nb) continue;
+            u32x8 w[R];
+            float wd[R];
+#pragma unroll
+            for (int s = 0; s < R; ++s) {
+                if (rows[s] >= 0) {
+                    w[s] = ld_stream_32B(p.w_qs + rows[s] * p.k + blk * QK);
+                    wd[s] = h2f(ld_nc_u16(p.w_d + rows[s] * p.nb + blk));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) w[s].v[i] = 0u;
+                    wd[s] = 0.0f;
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                if (b >= p.batch) break;
+                const int8_t *src = p.xq + static_cast<int64_t>(b) * p.k + blk * QK;
+                const uint4 lo = ld_16B(src);
+                const uint4 hi = ld_16B(src + 16);
+                const uint32_t xv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                const float xs = h2f(p.xd[static_cast<int64_t>(b) * p.nb + blk]);
+#pragma unroll
+                for (int s = 0; s < R; ++s) {
+                    int S = 0;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) S = dp4a(w[s].v[i], xv[i], S);
+                    acc[s][b] = fmaf(small_int_to_float(S), wd[s] * xs, acc[s][b]);
+                }
+            }
+        }
+        reduce_and_store<B, R>(p, t, lane, acc);
+    }
+}
+
+// Exact block sums s[b][n][j] (debug / parity export).  One thread per (b, n, j).
+__global__ void __launch_bounds__(256) block_dots_kernel(const int8_t *__restrict__ w_qs, int64_t n_rows, int k,
+                                                          const int8_t *__restrict__ xq, int batch,
+                                                          int32_t *__restrict__ s)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int nb = k / QK;
+    const int64_t total = static_cast<int64_t>(batch) * n_rows * nb;
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= total) return;
+    const int j = static_cast<int>(i % nb);
+    const int64_t n = (i / nb) % n_rows;
+    const int64_t b = i / (static_cast<int64_t>(nb) * n_rows);
+    const u32x8 w = ld_stream_32B(w_qs + n * k + j * QK);
+    const uint4 lo = ld_16B(xq + b * k + j * QK);
+    const uint4 hi = ld_16B(xq + b * k + j * QK + 16);
+    const uint32_t xv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    int acc = 0;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) acc = dp4a(w.v[t], xv[t], acc);
+    s[i] = acc;
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+// Resident CTAs per SM of one kernel, cached per kernel (function pointer).
+static int max_ctas_per_sm(const void *kernel)
+{
+    static std::mutex mu;
+    static std::unordered_map<const void *, int> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(kernel);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, GEMV_THREADS, 0) != cudaSuccess || n < 1) n = 1;
+    cache[kernel] = n;
+    return n;
+}
+
+static cudaError_t launch_gemv(void (*kernel)(GemvParams), const GemvParams &p, cudaStream_t s)
+{
+    const int occ = max_ctas_per_sm(reinterpret_cast<const void *>(kernel));
+    const int wpc = GEMV_THREADS / 32;
+    const int64_t need = (p.n_tasks + wpc - 1) / wpc;
+    const int64_t cap = static_cast<int64_t>(num_sms()) * occ;
+    const unsigned grid = static_cast<unsigned>(need < cap ? need : cap);
+    return launch_pdl(kernel, dim3(grid), dim3(GEMV_THREADS), 0, s, p);
+}
+
+template <int B, int R>
+static cudaError_t dispatch_nbl(const GemvParams &p, int nbl, cudaStream_t s)
+{
+    if constexpr (B == 1 || B == 2) {
+        switch (nbl) {
+        case 1: return launch_gemv(gemv_q8_0_reg_kernel<B, 1, R>, p, s);
+        case 2: return launch_gemv(gemv_q8_0_reg_kernel<B, 2, R>, p, s);
+        case 3: return launch_gemv(gemv_q8_0_reg_kernel<B, 3, R>, p, s);
+        case 4: return launch_gemv(gemv_q8_0_reg_kernel<B, 4, R>, p, s);
+        default: break;
+        }
+    } else if constexpr (B == 4) {
+        switch (nbl) {
+        case 1: return launch_gemv(gemv_q8_0_reg_kernel<B, 1, R>, p, s);
+        case 2: return launch_gemv(gemv_q8_0_reg_kernel<B, 2, R>, p, s);
+        default: break;
+        }
+    } else {
+        if (nbl == 1) return launch_gemv(gemv_q8_0_reg_kernel<B, 1, R>, p, s);
+    }
+    return launch_gemv(gemv_q8_0_generic_kernel<B, R>, p, s);
+}
+
+template <int B>
+static cudaError_t dispatch_r(GemvParams p, int nbl, cudaStream_t s)
+{
+    const bool silu = p.epi == QG_EPI_SILU_MUL_HALVES;
+    // Rows per warp task: as many as keep at least ~16 warps per SM busy.
+    const int64_t want_warps = static_cast<int64_t>(num_sms()) * 16;
+    int R = 4;
+    if (p.n_rows / 4 < want_warps) R = 2;
+    if (!silu && p.n_rows / 2 < want_warps) R = 1;
+    if (B >= 4 && R > 2) R = 2;  // register budget of the batched activation
+    const int64_t slots = p.n_rows;
+    p.n_tasks = (slots + R - 1) / R;
+    if (silu) p.n_tasks = (p.half + R / 2 - 1) / (R / 2);
+    switch (R) {
+    case 4: return dispatch_nbl<B, 4>(p, nbl, s);
+    case 2: return dispatch_nbl<B, 2>(p, nbl, s);
+    default: return dispatch_nbl<B, 1>(p, nbl, s);
+    }
+}
+
+cudaError_t launch_gemv_q8_0(const int8_t *w_qs, const uint16_t *w_d, int64_t n_rows, int64_t k, const int8_t *xq,
+                             const uint16_t *xd, int64_t batch, int epi, const float *residual, float *y,
+                             cudaStream_t s)
+{
+    if (n_rows == 0) return cudaSuccess;
+    GemvParams p;
+    p.w_qs = w_qs;
+    p.w_d = w_d;
+    p.xq = xq;
+    p.xd = xd;
+    p.residual = residual;
+    p.y = y;
+    p.n_rows = n_rows;
+    p.k = static_cast<int>(k);
+    p.nb = static_cast<int>(k / QK);
+    p.epi = epi;
+    p.half = n_rows / 2;
+    p.n_out = (epi == QG_EPI_SILU_MUL_HALVES) ? n_rows / 2 : n_rows;
+    p.n_tasks = 0;
+    p.batch = static_cast<int>(batch);
+    const int nbl = (p.nb + 31) / 32;
+    if (batch == 1) return dispatch_r<1>(p, nbl, s);
+    if (batch == 2) return dispatch_r<2>(p, nbl, s);
+    if (batch <= 4) return dispatch_r<4>(p, nbl, s);
+    if (batch <= 8) return dispatch_r<8>(p, nbl, s);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_block_dots(const int8_t *w_qs, int64_t n_rows, int64_t k, const int8_t *xq, int64_t batch,
+                              int32_t *s_out, cudaStream_t s)
+{
+    const int64_t total = batch * n_rows * (k / QK);
+    if (total == 0) return cudaSuccess;
+    const unsigned grid = static_cast<unsigned>((total + 255) / 256);
+    return launch_pdl(block_dots_kernel, dim3(grid), dim3(256), 0, s, w_qs, n_rows, static_cast<int>(k), xq,
+                      static_cast<int>(batch), s_out);
+}
+
+}  // namespace qg

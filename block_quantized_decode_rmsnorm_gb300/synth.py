@@ -38,6 +38,9 @@ convenience, directly as the two planes (values ``qs[n][k]``, scales
 
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 
 GOLDEN = np.uint64(0x9E3779B97F4A7C15)
@@ -48,7 +51,20 @@ _M2 = np.uint64(0x94D049BB133111EB)
 QK = 32  # values per Q8_0 block
 BLOCK_BYTES = 34  # fp16 scale + 32 int8 values
 
-_CHUNK = 1 << 22
+_CHUNK = 1 << 20
+_WORKERS = max(1, min(16, os.cpu_count() or 1))
+
+
+def _chunked(count: int, fn) -> None:
+    """Run fn(lo, hi) over [0, count) in chunks, on host threads when large
+    (every output depends only on its own counter, so chunks are independent)."""
+    spans = [(lo, min(count, lo + _CHUNK)) for lo in range(0, count, _CHUNK)]
+    if len(spans) <= 1 or _WORKERS == 1:
+        for lo, hi in spans:
+            fn(lo, hi)
+        return
+    with ThreadPoolExecutor(_WORKERS) as ex:
+        list(ex.map(lambda sp: fn(*sp), spans))
 
 
 def _mix64(z: np.ndarray) -> np.ndarray:
@@ -57,42 +73,70 @@ def _mix64(z: np.ndarray) -> np.ndarray:
     return z ^ (z >> np.uint64(31))
 
 
+def _base(seed: int, stream: int) -> np.uint64:
+    with np.errstate(over="ignore"):
+        return np.uint64(seed % (1 << 64)) * GOLDEN + np.uint64(stream % (1 << 64)) * STREAM_MUL
+
+
+def _raw(base: np.uint64, lo: int, hi: int) -> np.ndarray:
+    with np.errstate(over="ignore"):
+        ctr = np.arange(lo + 1, hi + 1, dtype=np.uint64)
+        return _mix64(base + ctr * GOLDEN)
+
+
 def raw_u64(seed: int, stream: int, count: int, offset: int = 0) -> np.ndarray:
     """Outputs ``offset .. offset+count-1`` of SplitMix64 stream (seed, stream)."""
-    with np.errstate(over="ignore"):
-        base = np.uint64(seed % (1 << 64)) * GOLDEN + np.uint64(stream % (1 << 64)) * STREAM_MUL
-        out = np.empty(count, dtype=np.uint64)
-        for lo in range(0, count, _CHUNK):
-            hi = min(count, lo + _CHUNK)
-            ctr = np.arange(offset + lo + 1, offset + hi + 1, dtype=np.uint64)
-            out[lo:hi] = _mix64(base + ctr * GOLDEN)
+    base = _base(seed, stream)
+    out = np.empty(count, dtype=np.uint64)
+
+    def fill(lo, hi):
+        out[lo:hi] = _raw(base, offset + lo, offset + hi)
+
+    _chunked(count, fill)
     return out
 
 
 def uniform01(seed: int, stream: int, count: int) -> np.ndarray:
     """f64 uniforms in [0, 1) with 53 random bits each."""
-    z = raw_u64(seed, stream, count)
-    return (z >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+    base = _base(seed, stream)
+    out = np.empty(count, dtype=np.float64)
+
+    def fill(lo, hi):
+        out[lo:hi] = (_raw(base, lo, hi) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+
+    _chunked(count, fill)
+    return out
 
 
 def uniform_int(seed: int, stream: int, count: int, lo: int, hi: int) -> np.ndarray:
     """Integers uniform in [lo, hi] (inclusive) as int64."""
+    base = _base(seed, stream)
     span = np.uint64(hi - lo + 1)
     out = np.empty(count, dtype=np.int64)
-    for c0 in range(0, count, _CHUNK):
-        c1 = min(count, c0 + _CHUNK)
-        z = raw_u64(seed, stream, c1 - c0, offset=c0)
+
+    def fill(a, b):
+        z = _raw(base, a, b)
         with np.errstate(over="ignore"):
             v = ((z >> np.uint64(32)) * span) >> np.uint64(32)
-        out[c0:c1] = v.astype(np.int64) + lo
+        out[a:b] = v.astype(np.int64) + lo
+
+    _chunked(count, fill)
     return out
 
 
 def normal(seed: int, stream: int, count: int, mean: float = 0.0, std: float = 1.0) -> np.ndarray:
-    """f64 normals by Box-Muller over consecutive uniform pairs."""
-    u = uniform01(seed, stream, 2 * count).reshape(count, 2)
-    rad = np.sqrt(-2.0 * np.log1p(-u[:, 0]))
-    return mean + std * rad * np.cos(2.0 * np.pi * u[:, 1])
+    """f64 normals by Box-Muller over consecutive uniform pairs (outputs 2i, 2i+1)."""
+    base = _base(seed, stream)
+    out = np.empty(count, dtype=np.float64)
+
+    def fill(a, b):
+        z = _raw(base, 2 * a, 2 * b)
+        u = ((z >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)).reshape(b - a, 2)
+        rad = np.sqrt(-2.0 * np.log1p(-u[:, 0]))
+        out[a:b] = mean + std * rad * np.cos(2.0 * np.pi * u[:, 1])
+
+    _chunked(count, fill)
+    return out
 
 
 # --------------------------------------------------------------------------

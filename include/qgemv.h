@@ -1,0 +1,184 @@
+/*
+ * qgemv.h - C ABI of libqgemv.so: the weight-streaming matrix-vector product of
+ * an LLM decode step over Q8_0 block-quantized weights, its bf16 variant, the
+ * activation quantizers that feed it, and the prompt-sized (M rows) form of the
+ * same contraction.  GB300 (sm_103a) only.
+ *
+ * Sources (web pages; sections as named on the page):
+ *   [Phobos]  "Filling in the blanks: Inference using Phobos"
+ *   [Herbert] "One level down: #002 the same compiler on a GPU"
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *   never allocates, frees or synchronises inside these calls and reads no
+ *   environment variable, so every call can be recorded into a CUDA graph.
+ * - Sizes are element counts.  K (the reduction length) must be a positive
+ *   multiple of 32 for Q8_0 data.  A size of 0 rows is valid and launches nothing.
+ * - Q8_0 weights are held as two planes ("packed layout"): values
+ *   qs[n_rows][k] (int8, row-major) and scales d[n_rows][k/32] (IEEE binary16
+ *   bit patterns, row-major).  qg_q8_0_pack converts the canonical 34-byte
+ *   block layout into these planes.
+ * - Q8_0 activations use the same two planes: q[rows][k] and d[rows][k/32].
+ * - Alignment: weight value planes (qs) must be 32-byte aligned; every other
+ *   pointer 16-byte aligned, except binary16 scale planes (2-byte aligned).
+ * - Calls are asynchronous in the order of `stream` (NULL = legacy default
+ *   stream).  Kernels are launched with programmatic dependent launch: a kernel
+ *   may start streaming its WEIGHTS while the previous kernel in the stream
+ *   finishes, and reads activations only after that kernel has completed.
+ *   Weights must therefore not be written by a kernel that is still running
+ *   when the call is made (writes by qg_q8_0_pack or by any kernel that has
+ *   completed are fine).
+ * - Errors: argument errors are returned before anything is launched; a
+ *   launch failure returns QG_ERR_CUDA.  Errors inside the kernels are not
+ *   reported by these calls (the kernels have no failing paths on valid input).
+ * - Outputs never alias inputs, except where a call says so.
+ * - Thread-safe; no global state.
+ */
+#ifndef QGEMV_H
+#define QGEMV_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QG_API __attribute__((visibility("default")))
+#else
+#define QG_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st *qg_stream_t;
+
+typedef enum {
+    QG_OK = 0,
+    QG_ERR_NULL = 1,        /* a required pointer is NULL */
+    QG_ERR_ALIGN = 2,       /* a pointer breaks the alignment rule above */
+    QG_ERR_SHAPE = 3,       /* a size is negative, not a multiple of 32, or too large */
+    QG_ERR_UNSUPPORTED = 4, /* valid request this build does not serve (e.g. batch > 8) */
+    QG_ERR_CUDA = 5         /* the CUDA runtime reported an error at launch */
+} qg_status;
+
+/* Epilogues fused into the GEMV ([Phobos] Fast Decode: fold the residual add
+ * into the matmul; [Herbert] Emitting for a GPU: the activation is fused with
+ * the projection). */
+typedef enum {
+    QG_EPI_NONE = 0,            /* y[b][n] = dot(W[n], x[b]) */
+    QG_EPI_SILU_MUL_HALVES = 1, /* n_rows even, F = n_rows/2, rows [0,F) gate, [F,2F) up:
+                                   y[b][i] = silu(g_i) * u_i, silu(g) = g / (1 + e^-g),
+                                   y has F columns per batch row */
+    QG_EPI_RESIDUAL_ADD = 2     /* y[b][n] = residual[b][n] + dot(W[n], x[b]);
+                                   residual may be the same buffer as y */
+} qg_epilogue;
+
+/* Human-readable name of a status. */
+QG_API const char *qg_status_str(qg_status s);
+
+/* ABI version of this header (bumped on any signature change). */
+QG_API int qg_abi_version(void);
+
+/*
+ * qg_q8_0_pack - canonical Q8_0 blocks -> packed planes.
+ * [Phobos] GPU Performance Heisenbugs: weights are stored so that a decode warp
+ * reads whole cache lines.  Canonical block: 2-byte little-endian binary16 scale
+ * followed by 32 int8 values (34 bytes); blocks[n_rows][k/32].
+ *   blocks: device, 1-byte aligned, n_rows*(k/32)*34 bytes (read)
+ *   qs:     device, 32-byte aligned, int8[n_rows][k] (written)
+ *   d:      device, binary16 bits uint16[n_rows][k/32] (written)
+ * A byte permutation; a one-time load step, not part of the decode step.
+ */
+QG_API qg_status qg_q8_0_pack(const void *blocks, int64_t n_rows, int64_t k,
+                       int8_t *qs, uint16_t *d, qg_stream_t stream);
+
+/*
+ * quantize_act_q8_0 - quantize activations to Q8_0, once, to be shared by
+ * every projection that reads them ([Phobos] Fast Decode).
+ * Per 32-value block: d = max|x| / 127 (f32), q = round half away from zero of
+ * x / d (one IEEE f32 division; d == 0 gives q = 0), clamped to [-127, 127];
+ * the stored scale is binary16(d), round to nearest even.
+ *   x: device f32[rows][k] (read)
+ *   q: device int8[rows][k] (written)      d: device binary16 bits [rows][k/32] (written)
+ */
+QG_API qg_status quantize_act_q8_0(const float *x, int64_t rows, int64_t k,
+                            int8_t *q, uint16_t *d, qg_stream_t stream);
+
+/*
+ * rmsnorm_quantize - RMSNorm followed by Q8_0 quantization of each row.
+ * [Herbert] Emitting for a GPU (normalization fused with the projection that
+ * follows it); [Phobos] Q4_K_M (the fast norm kernel).
+ *   r = 1 / sqrt(mean_k(x^2) + eps), evaluated in f64 and rounded once to f32;
+ *   x_hat = (x * r) * gamma (two f32 multiplies); then quantize_act_q8_0(x_hat).
+ *   x:       device f32[rows][k] (read)     gamma: device f32[k] (read)
+ *   q, d:    as quantize_act_q8_0 (written)
+ *   inv_rms: device f32[rows] receiving r, or NULL
+ *   k <= 65536.
+ */
+QG_API qg_status rmsnorm_quantize(const float *x, const float *gamma, int64_t rows, int64_t k,
+                           float eps, int8_t *q, uint16_t *d, float *inv_rms,
+                           qg_stream_t stream);
+
+/*
+ * qgemv_q8_0 - block-scaled Q8_0 matrix-vector product ([Phobos] Fast Decode:
+ * int8 dot products end to end, one scale per 32 values, a warp owns an output
+ * row and reduces with shuffles).
+ *   acc[b][n] = sum over blocks j of f32(d_w[n][j]) * f32(d_x[b][j]) * S_j,
+ *   S_j = exact int32 sum of w_qs[n][32j+i] * xq[b][32j+i], i < 32;
+ *   accumulation in f32 (order unspecified), then the epilogue.
+ *   w_qs, w_d: packed weight planes [n_rows][k], [n_rows][k/32] (read)
+ *   xq, xd:    Q8_0 activations [batch][k], [batch][k/32] (read)
+ *   batch:     1 <= batch <= 8 (batch rows share one pass over the weights)
+ *   epilogue:  a qg_epilogue; residual: device f32[batch][n_rows] for
+ *              QG_EPI_RESIDUAL_ADD (may equal y), else ignored
+ *   y:         device f32[batch][n_out], n_out = n_rows, or n_rows/2 for
+ *              QG_EPI_SILU_MUL_HALVES (written)
+ */
+QG_API qg_status qgemv_q8_0(const int8_t *w_qs, const uint16_t *w_d, int64_t n_rows, int64_t k,
+                     const int8_t *xq, const uint16_t *xd, int64_t batch,
+                     int epilogue, const float *residual, float *y, qg_stream_t stream);
+
+/*
+ * qgemv_bf16 - bf16-weight matrix-vector product with f32 accumulation
+ * ([Herbert] The numerical contract; Emitting for a GPU: rows read as 16-byte
+ * groups of eight bf16, norm fused in front, activation fused behind).
+ *   With gamma != NULL: r = 1/sqrt(mean(x^2)+eps) (f64, rounded to f32),
+ *   x_hat = bf16_rne((x * r) * gamma); with gamma == NULL: x_hat = x.
+ *   acc[n] = sum_k f32(w[n][k]) * f32(x_hat[k]) in f32, then the epilogue
+ *   (QG_EPI_NONE, QG_EPI_SILU_MUL_HALVES or QG_EPI_RESIDUAL_ADD as above).
+ *   w: device bf16 bits [n_rows][k] (read), k a multiple of 8, k <= 16384
+ *   x, gamma: device bf16 bits [k] (read)
+ *   y: device f32[n_out] (written)
+ */
+QG_API qg_status qgemv_bf16(const uint16_t *w, int64_t n_rows, int64_t k, const uint16_t *x,
+                     const uint16_t *gamma, float eps, int epilogue,
+                     const float *residual, float *y, qg_stream_t stream);
+
+/*
+ * qgemm_q8_0_prefill - the same block-scaled contraction for M prompt rows
+ * ([Phobos] Fast Decode: prompt processing reuses every weight M times and
+ * belongs on the tensor cores; GPU Performance Heisenbugs: exact int8 values
+ * run straight on the integer tensor cores).
+ *   Y[m][n] = sum_j f32(d_x[m][j]) * f32(d_w[n][j]) * S_j[m][n], f32 accumulation.
+ *   xq, xd: Q8_0 activations [m][k], [m][k/32]; w_qs, w_d: packed weights.
+ *   y: device f32[m][n_rows] (written)
+ */
+QG_API qg_status qgemm_q8_0_prefill(const int8_t *w_qs, const uint16_t *w_d, int64_t n_rows,
+                             int64_t k, const int8_t *xq, const uint16_t *xd, int64_t m,
+                             float *y, qg_stream_t stream);
+
+/*
+ * qg_debug_block_dots_q8_0 - the exact per-block int32 sums, for parity checks.
+ *   s[b][n][j] = sum_{i<32} w_qs[n][32j+i] * xq[b][32j+i]   (int32, exact)
+ *   s: device int32[batch][n_rows][k/32] (written); batch <= 8.
+ */
+QG_API qg_status qg_debug_block_dots_q8_0(const int8_t *w_qs, int64_t n_rows, int64_t k,
+                                   const int8_t *xq, int64_t batch, int32_t *s,
+                                   qg_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMV_H */

@@ -1,0 +1,100 @@
+"""CPU checks of the C ABI: the library builds, loads, exports every symbol
+include/qgemv.h declares, and rejects bad arguments before touching CUDA.
+
+No call here reaches a kernel: every argument error is detected on the host
+before any CUDA runtime call, which is what lets these run without a GPU.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qgemv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_quantized_decode_rmsnorm_gb300 import _lib, build
+
+    build()
+    return _lib.load()
+
+
+def _declared():
+    src = open(HEADER).read()
+    return re.findall(r"QG_API\s+[\w\s\*]+?\b(\w+)\s*\(", src)
+
+
+def test_header_declares_the_boundary():
+    names = set(_declared())
+    for need in ["qgemv_q8_0", "qgemv_bf16", "quantize_act_q8_0", "rmsnorm_quantize", "qgemm_q8_0_prefill",
+                 "qg_q8_0_pack", "qg_debug_block_dots_q8_0", "qg_status_str", "qg_abi_version"]:
+        assert need in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from block_quantized_decode_rmsnorm_gb300 import _lib
+
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"binding lacks {name}"
+    assert lib.qg_abi_version() == 1
+
+
+def test_status_strings(lib):
+    assert lib.qg_status_str(0) == b"ok"
+    assert lib.qg_status_str(3) == b"bad shape"
+    assert lib.qg_status_str(99) == b"unknown status"
+
+
+FAKE = 1 << 20  # a well-aligned, never-dereferenced address
+
+
+def test_gemv_argument_errors(lib):
+    q = lib.qgemv_q8_0
+    # K not a multiple of 32
+    assert q(FAKE, FAKE, 8, 48, FAKE, FAKE, 1, 0, None, FAKE, None) == 3
+    # negative rows, zero batch
+    assert q(FAKE, FAKE, -1, 64, FAKE, FAKE, 1, 0, None, FAKE, None) == 3
+    assert q(FAKE, FAKE, 8, 64, FAKE, FAKE, 0, 0, None, FAKE, None) == 3
+    # batch beyond what the kernels serve
+    assert q(FAKE, FAKE, 8, 64, FAKE, FAKE, 9, 0, None, FAKE, None) == 4
+    # unknown epilogue
+    assert q(FAKE, FAKE, 8, 64, FAKE, FAKE, 1, 7, None, FAKE, None) == 4
+    # odd rows for the stacked-halves epilogue
+    assert q(FAKE, FAKE, 7, 64, FAKE, FAKE, 1, 1, None, FAKE, None) == 3
+    # null pointers
+    assert q(None, FAKE, 8, 64, FAKE, FAKE, 1, 0, None, FAKE, None) == 1
+    assert q(FAKE, FAKE, 8, 64, FAKE, FAKE, 1, 2, None, FAKE, None) == 1  # residual missing
+    # weight values must be 32-byte aligned, activations 16
+    assert q(FAKE + 16, FAKE, 8, 64, FAKE, FAKE, 1, 0, None, FAKE, None) == 2
+    assert q(FAKE, FAKE, 8, 64, FAKE + 8, FAKE, 1, 0, None, FAKE, None) == 2
+    # zero rows is a valid no-op (nothing launched)
+    assert q(None, None, 0, 64, None, None, 1, 0, None, None, None) == 0
+
+
+def test_other_argument_errors(lib):
+    assert lib.quantize_act_q8_0(FAKE, 1, 33, FAKE, FAKE, None) == 3
+    assert lib.quantize_act_q8_0(None, 1, 32, FAKE, FAKE, None) == 1
+    assert lib.quantize_act_q8_0(FAKE + 4, 1, 32, FAKE, FAKE, None) == 2
+    assert lib.quantize_act_q8_0(None, 0, 32, None, None, None) == 0
+    assert lib.rmsnorm_quantize(FAKE, FAKE, 1, 65536 + 32, ctypes.c_float(1e-6), FAKE, FAKE, None, None) == 3
+    assert lib.rmsnorm_quantize(FAKE, FAKE, 1, 64, ctypes.c_float(-1.0), FAKE, FAKE, None, None) == 3
+    assert lib.rmsnorm_quantize(FAKE, None, 1, 64, ctypes.c_float(1e-6), FAKE, FAKE, None, None) == 1
+    assert lib.qgemv_bf16(FAKE, 8, 12, FAKE, None, ctypes.c_float(0.0), 0, None, FAKE, None) == 3
+    assert lib.qgemv_bf16(FAKE + 8, 8, 16, FAKE, None, ctypes.c_float(0.0), 0, None, FAKE, None) == 2
+    assert lib.qgemm_q8_0_prefill(FAKE, FAKE, 8, 64, FAKE, FAKE, -1, FAKE, None) == 3
+    assert lib.qgemm_q8_0_prefill(FAKE, FAKE, 8, 64, FAKE, FAKE, 0, FAKE, None) == 0
+    assert lib.qg_q8_0_pack(FAKE, 4, 64, FAKE + 16, FAKE, None) == 2
+    assert lib.qg_debug_block_dots_q8_0(FAKE, 4, 64, FAKE, 9, FAKE, None) == 3
+
+
+def test_binding_refuses_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    from block_quantized_decode_rmsnorm_gb300 import api
+
+    with pytest.raises(ValueError, match="CUDA"):
+        api.quantize_act_q8_0(torch.zeros(1, 32))
