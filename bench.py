@@ -43,8 +43,8 @@ EPS = 1e-6
 W_GU_BYTES = 2 * FFN * HIDDEN + 2 * FFN * (HIDDEN // 32) * 2
 W_DN_BYTES = HIDDEN * FFN + HIDDEN * (FFN // 32) * 2
 LAYER_BYTES = W_GU_BYTES + W_DN_BYTES + 3 * HIDDEN * 4
-# gate|up GEMV per launch: weights, Q8_0 input (values + scales), h out (f32)
-GU_KERNEL_BYTES = W_GU_BYTES + HIDDEN + (HIDDEN // 32) * 2 + FFN * 4
+# fused gate|up launch: weights, x and gamma in (f32), h out (f32) and its Q8_0 codes + scales
+GU_KERNEL_BYTES = W_GU_BYTES + 2 * HIDDEN * 4 + FFN * 4 + FFN + (FFN // 32) * 2
 
 
 def workload_name(layers: int) -> str:
@@ -303,7 +303,7 @@ def ncu_traffic(kernel_key: str):
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("qg_gemv.cu", "qg_common.cuh"):
+    for f in ("qg_ffn.cu", "qg_norm.cuh", "qg_common.cuh"):
         with open(os.path.join(ROOT, "block_quantized_decode_rmsnorm_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
@@ -347,9 +347,15 @@ def run_ours(args):
     buf = api.FFNBuffers.allocate(HIDDEN, FFN, "cuda")
     x = torch.from_numpy(x0_np).cuda()
 
+    fused = not args.unfused
+    launches_per_layer = 2 if fused else 4
+
     def step():
         for layer in layers:
-            api.decode_ffn_q8_0(x, layer, buf, EPS)
+            if fused:
+                api.qg_decode_ffn_q8_0(x, layer, buf, EPS)
+            else:
+                api.decode_ffn_q8_0(x, layer, buf, EPS)
 
     g = capture(torch, step)
     for _ in range(args.warmup):
@@ -372,15 +378,16 @@ def run_ours(args):
     step_bytes = L * LAYER_BYTES
     value = dist.world * args.steps * step_bytes / elapsed / 1e9
 
-    # dominant kernel: the gate|up GEMV, launched back to back over the L layers
-    gu_graph = capture(torch, lambda: [api.qgemv_q8_0(l.gate_up, buf.xq, buf.xd, epilogue="silu_mul", y=buf.h)
+    # dominant kernel: the fused gate|up launch, back to back over the L layers
+    h1, hq1, hd1 = buf.h[0], buf.hq[0], buf.hd[0]
+    gu_graph = capture(torch, lambda: [api.qg_ffn_up_q8_0(x, l.gamma, l.gate_up, EPS, h=h1, hq=hq1, hd=hd1)
                                        for l in layers])
     t_gu = time_graph(torch, gu_graph, max(5, args.steps // 4)) / L
     achieved = GU_KERNEL_BYTES / t_gu / 1e9
-    roofline = {"bound": "hbm", "kernel": "gemv_q8_0_reg_kernel<1,1,2> (gate|up 7168x1024, SiLU*u)",
+    roofline = {"bound": "hbm", "kernel": "ffn_up_kernel<1> (RMSNorm + Q8_0 + gate|up 7168x1024 + SiLU*u + Q8_0)",
                 "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
                 "peak_source": pk["source"], "algorithmic_bytes_per_launch": GU_KERNEL_BYTES,
-                "launch_us": t_gu * 1e6, "traffic": ncu_traffic("gemv_q8_0_gate_up")}
+                "launch_us": t_gu * 1e6, "traffic": ncu_traffic("ffn_up_kernel")}
     del gu_graph
 
     # end to end through host buffers: H2D of x, the step, D2H of the result, every step
@@ -411,9 +418,10 @@ def run_ours(args):
                    "frac_of_hbm_peak": value / dist.world / pk["hbm_gbs"],
                    "l2": f"inputs larger than L2: {step_bytes / 1e6:.0f} MB of weights per step, "
                          f"L2 {torch.cuda.get_device_properties(dev).L2_cache_size / 1e6:.0f} MB",
-                   "graph": f"one CUDA graph per step, {4 * L} launches, programmatic dependent launch",
+                   "graph": f"one CUDA graph per step, {launches_per_layer * L} launches, programmatic dependent launch",
+                   "path": "fused (qg_decode_ffn_q8_0)" if fused else "unfused (4 launches per layer)",
                    "parallelism": f"replicas x{dist.world} (independent decode streams, no collective)"},
-        "roofline": roofline, "e2e": e2e, "gpu_launches": 4 * L * args.steps, "clocks": clocks,
+        "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_layer * L * args.steps, "clocks": clocks,
     }
     if not args.quick:
         line["other_workloads"] = extra_configs(torch, pk)
@@ -477,6 +485,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layers", type=int, default=24)
     ap.add_argument("--quick", action="store_true", help="skip the other workloads' kernel rates")
+    ap.add_argument("--unfused", action="store_true", help="time the four-launch composition instead")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     if args.warmup < 3:

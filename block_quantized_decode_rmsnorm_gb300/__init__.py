@@ -8,7 +8,8 @@ library; the binding's names resolve on first use.
 
 _API_NAMES = {
     "qg_q8_0_pack", "quantize_act_q8_0", "rmsnorm_quantize", "qgemv_q8_0", "qgemv_bf16",
-    "qgemm_q8_0_prefill", "qg_debug_block_dots_q8_0", "decode_ffn_q8_0", "Q8Weight", "FFNLayer",
+    "qgemm_q8_0_prefill", "qg_debug_block_dots_q8_0", "decode_ffn_q8_0", "qg_ffn_up_q8_0",
+    "qg_decode_ffn_q8_0", "Q8Weight", "FFNLayer",
     "FFNBuffers", "q8_weight_from_numpy", "bf16_from_bits",
 }
 
@@ -23,6 +24,6 @@ def __getattr__(name):
 
 def build(force: bool = False) -> str:
     """Compile libqgemv.so in-tree (nvcc, sm_103a)."""
-    from .build import build as _build
+    from .builder import build as _build
 
     return _build(force=force)

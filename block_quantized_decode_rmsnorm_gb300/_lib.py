@@ -32,6 +32,8 @@ SIGNATURES = {
     "qgemv_q8_0": (ST, [P, P, I64, I64, P, P, I64, I32, P, P, P]),
     "qgemv_bf16": (ST, [P, I64, I64, P, P, F32, I32, P, P, P]),
     "qgemm_q8_0_prefill": (ST, [P, P, I64, I64, P, P, I64, P, P]),
+    "qg_ffn_up_q8_0": (ST, [P, P, I64, F32, P, P, I64, P, P, P, P, P, P, P]),
+    "qg_decode_ffn_q8_0": (ST, [P, P, I64, I64, F32, P, P, P, P, P, P, P, P]),
     "qg_debug_block_dots_q8_0": (ST, [P, I64, I64, P, I64, P, P]),
 }
 
@@ -54,7 +56,7 @@ def load(path: str | None = None):
             if not os.path.exists(p):
                 raise RuntimeError(
                     f"libqgemv.so not found at {p}: build it first "
-                    "(python -m block_quantized_decode_rmsnorm_gb300.build, or __graft_entry__.build())")
+                    "(python -m block_quantized_decode_rmsnorm_gb300.builder, or __graft_entry__.build())")
             lib = ctypes.CDLL(p)
             for name, (res, args) in SIGNATURES.items():
                 fn = getattr(lib, name)

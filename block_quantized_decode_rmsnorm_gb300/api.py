@@ -262,6 +262,42 @@ def decode_ffn_q8_0(x: torch.Tensor, layer: FFNLayer, buf: FFNBuffers, eps: floa
               buf.hd.data_ptr(), 1, QG_EPI_RESIDUAL_ADD, x.data_ptr(), x.data_ptr(), s)
 
 
+def qg_ffn_up_q8_0(x: torch.Tensor, gamma: torch.Tensor, w: Q8Weight, eps: float = 1e-6, h=None, hq=None, hd=None,
+                   xq_out=None, xd_out=None, inv_rms_out=None, stream=None):
+    """RMSNorm -> Q8_0 -> stacked gate|up -> SiLU(g)*u -> (h, hq, hd), one launch."""
+    hidden = x.shape[-1]
+    _need(x, "x", torch.float32, (hidden,))
+    _need(gamma, "gamma", torch.float32, (hidden,))
+    _need(w.qs, "w.qs", torch.int8)
+    n_rows = w.qs.shape[0]
+    ffn = n_rows // 2
+    _need(w.qs, "w.qs", torch.int8, (2 * ffn, hidden))
+    _need(w.d, "w.d", torch.float16, (2 * ffn, hidden // 32))
+    dev = x.device
+    if h is None:
+        h = torch.empty((ffn,), dtype=torch.float32, device=dev)
+    if hq is None:
+        hq = torch.empty((ffn,), dtype=torch.int8, device=dev)
+    if hd is None:
+        hd = torch.empty((ffn // 32,), dtype=torch.float16, device=dev)
+    _need(h, "h", torch.float32, (ffn,))
+    _need(hq, "hq", torch.int8, (ffn,))
+    _need(hd, "hd", torch.float16, (ffn // 32,))
+    _lib.call("qg_ffn_up_q8_0", x.data_ptr(), gamma.data_ptr(), hidden, float(eps), w.qs.data_ptr(), w.d.data_ptr(),
+              ffn, h.data_ptr(), hq.data_ptr(), hd.data_ptr(), _ptr(xq_out), _ptr(xd_out), _ptr(inv_rms_out),
+              _stream_handle(stream))
+    return h, hq, hd
+
+
+def qg_decode_ffn_q8_0(x: torch.Tensor, layer: FFNLayer, buf: FFNBuffers, eps: float = 1e-6, stream=None) -> None:
+    """x <- x + down(SiLU(g)*u) in two launches (fused gate|up, then down + residual)."""
+    hidden = x.shape[-1]
+    ffn = layer.down.k
+    _lib.call("qg_decode_ffn_q8_0", x.data_ptr(), layer.gamma.data_ptr(), hidden, ffn, float(eps),
+              layer.gate_up.qs.data_ptr(), layer.gate_up.d.data_ptr(), layer.down.qs.data_ptr(),
+              layer.down.d.data_ptr(), buf.h.data_ptr(), buf.hq.data_ptr(), buf.hd.data_ptr(), _stream_handle(stream))
+
+
 # --------------------------------------------------------------------------
 # host <-> device helpers (plumbing)
 # --------------------------------------------------------------------------

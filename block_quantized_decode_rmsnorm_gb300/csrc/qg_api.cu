@@ -17,6 +17,12 @@ cudaError_t launch_gemv_bf16(const uint16_t *, int64_t, int64_t, const uint16_t 
                              const float *, float *, cudaStream_t);
 cudaError_t launch_prefill_mma(const int8_t *, const uint16_t *, int64_t, int64_t, const int8_t *, const uint16_t *,
                                int64_t, float *, cudaStream_t);
+bool ffn_up_supported(int64_t k, int64_t half);
+cudaError_t launch_ffn_up(const float *, const float *, int64_t, float, const int8_t *, const uint16_t *, int64_t,
+                          float *, int8_t *, uint16_t *, int8_t *, uint16_t *, float *, cudaStream_t);
+bool prefetch_supported(int64_t n_rows, int64_t k);
+cudaError_t launch_gemv_prefetch(const int8_t *, const uint16_t *, int64_t, int64_t, const int8_t *, const uint16_t *,
+                                 int, const float *, float *, cudaStream_t);
 
 // SM count of the current device, read once per device.
 int num_sms()
@@ -125,6 +131,11 @@ qg_status qgemv_q8_0(const int8_t *w_qs, const uint16_t *w_d, int64_t n_rows, in
     if (!aligned(w_qs, 32) || !aligned(w_d, 2) || !aligned(xq, 16) || !aligned(xd, 2) || !aligned(y, 16))
         return QG_ERR_ALIGN;
     if (epilogue == QG_EPI_RESIDUAL_ADD && !aligned(residual, 16)) return QG_ERR_ALIGN;
+    // Batch-1 products whose weights fit in one wave's registers take the
+    // prefetching kernel; everything else streams.
+    if (batch == 1 && epilogue != QG_EPI_SILU_MUL_HALVES && aligned(w_d, 16) &&
+        qg::prefetch_supported(n_rows, k))
+        return from_cuda(qg::launch_gemv_prefetch(w_qs, w_d, n_rows, k, xq, xd, epilogue, residual, y, stream));
     return from_cuda(qg::launch_gemv_q8_0(w_qs, w_d, n_rows, k, xq, xd, batch, epilogue, residual, y, stream));
 }
 
@@ -156,6 +167,44 @@ qg_status qgemm_q8_0_prefill(const int8_t *w_qs, const uint16_t *w_d, int64_t n_
     if (!aligned(w_qs, 32) || !aligned(w_d, 2) || !aligned(xq, 16) || !aligned(xd, 2) || !aligned(y, 16))
         return QG_ERR_ALIGN;
     return from_cuda(qg::launch_prefill_mma(w_qs, w_d, n_rows, k, xq, xd, m, y, stream));
+}
+
+qg_status qg_ffn_up_q8_0(const float *x, const float *gamma, int64_t hidden, float eps, const int8_t *w_qs,
+                         const uint16_t *w_d, int64_t ffn, float *h, int8_t *hq, uint16_t *hd, int8_t *xq_out,
+                         uint16_t *xd_out, float *inv_rms_out, qg_stream_t stream)
+{
+    if (hidden <= 0 || hidden % 32 != 0 || ffn < 0 || ffn % 32 != 0 || ffn > kMaxRows / 2) return QG_ERR_SHAPE;
+    if (hq && !aligned(hq, 32)) return QG_ERR_ALIGN;
+    if (!(eps >= 0.0f)) return QG_ERR_SHAPE;
+    if (!qg::ffn_up_supported(hidden, ffn)) return QG_ERR_UNSUPPORTED;
+    if (ffn == 0) return QG_OK;
+    if (!x || !gamma || !w_qs || !w_d || !h || !hq || !hd) return QG_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(gamma, 16) || !aligned(w_qs, 32) || !aligned(w_d, 16) || !aligned(h, 16) ||
+        !aligned(hq, 16) || !aligned(hd, 2) || !aligned(xq_out, 16) || !aligned(xd_out, 2) || !aligned(inv_rms_out, 4))
+        return QG_ERR_ALIGN;
+    return from_cuda(qg::launch_ffn_up(x, gamma, hidden, eps, w_qs, w_d, ffn, h, hq, hd, xq_out, xd_out, inv_rms_out,
+                                       stream));
+}
+
+qg_status qg_decode_ffn_q8_0(float *x, const float *gamma, int64_t hidden, int64_t ffn, float eps,
+                             const int8_t *wgu_qs, const uint16_t *wgu_d, const int8_t *wdn_qs,
+                             const uint16_t *wdn_d, float *h, int8_t *hq, uint16_t *hd, qg_stream_t stream)
+{
+    if (hidden <= 0 || hidden % 32 != 0 || ffn <= 0 || ffn % 32 != 0 || ffn > kMaxRows / 2 || ffn > kMaxK)
+        return QG_ERR_SHAPE;
+    if (!(eps >= 0.0f)) return QG_ERR_SHAPE;
+    if (!qg::ffn_up_supported(hidden, ffn)) return QG_ERR_UNSUPPORTED;
+    if (!x || !gamma || !wgu_qs || !wgu_d || !wdn_qs || !wdn_d || !h || !hq || !hd) return QG_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(gamma, 16) || !aligned(wgu_qs, 32) || !aligned(wgu_d, 16) ||
+        !aligned(wdn_qs, 32) || !aligned(wdn_d, 16) || !aligned(h, 16) || !aligned(hq, 32) || !aligned(hd, 2))
+        return QG_ERR_ALIGN;
+    qg_status st = from_cuda(qg::launch_ffn_up(x, gamma, hidden, eps, wgu_qs, wgu_d, ffn, h, hq, hd, nullptr,
+                                               nullptr, nullptr, stream));
+    if (st != QG_OK) return st;
+    if (qg::prefetch_supported(hidden, ffn) && aligned(wdn_d, 16))
+        return from_cuda(qg::launch_gemv_prefetch(wdn_qs, wdn_d, hidden, ffn, hq, hd, QG_EPI_RESIDUAL_ADD, x, x,
+                                                  stream));
+    return from_cuda(qg::launch_gemv_q8_0(wdn_qs, wdn_d, hidden, ffn, hq, hd, 1, QG_EPI_RESIDUAL_ADD, x, x, stream));
 }
 
 qg_status qg_debug_block_dots_q8_0(const int8_t *w_qs, int64_t n_rows, int64_t k, const int8_t *xq, int64_t batch,

@@ -115,9 +115,32 @@ __device__ __forceinline__ int q8_code(float v, float d)
     return static_cast<int>(t);
 }
 
+// silu(g) * u with silu(g) = g / (1 + e^-g).  For g < 0 the same value is
+// formed as (g e)(e) / (1 + e e) with e = e^(g/2): e^-g cannot overflow, and
+// the product g e^g stays representable even where e^g alone would underflow.
 __device__ __forceinline__ float silu_mul(float g, float u)
 {
-    return __fdiv_rn(g, 1.0f + expf(-g)) * u;
+    float s;
+    if (g >= 0.0f) {
+        s = __fdiv_rn(g, 1.0f + expf(-g));
+    } else {
+        const float e = expf(0.5f * g);
+        s = __fdiv_rn((g * e) * e, __fmaf_rn(e, e, 1.0f));
+    }
+    return s * u;
+}
+
+// 16-byte asynchronous global -> shared copy (LDGSTS); src and dst 16-byte aligned.
+__device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
 }  // namespace qg

@@ -1,0 +1,430 @@
+// Decode-step kernels whose whole weight slab is requested before they wait on
+// the kernel that produces their input.
+//
+// "Filling in the blanks: Inference using Phobos", Fast Decode: decode is a
+// pure weight stream; the activation is quantized once and shared, projections
+// that read it are stacked, the residual add is folded into the matmul, and the
+// pass is replayed as a graph.  "One level down: #002 the same compiler on a
+// GPU", Emitting for a GPU: the normalization is fused with the projection that
+// follows it and the activation with the projection before it.
+//
+// GB300 design.  A decode FFN layer moves 11.7 MB, about 1.7 us of HBM time,
+// but it is a chain of dependent steps (norm -> gate|up -> down) each of which
+// needs a full reduction of its predecessor's output.  Launched as separate
+// grids, every step pays launch ramp-up plus one DRAM round trip before its
+// weights arrive.  Here each kernel is a single wave whose CTAs copy their whole
+// weight slab (values, scales, gain) into shared memory with cp.async issued
+// BEFORE griddepcontrol.wait (~30-75 KB per CTA), and trigger their dependent
+// launch on entry.  Kernels further down the stream therefore become resident
+// and stream their weights while their predecessors still compute; after the
+// wait only on-chip work remains.  (Plain loads into registers would not do:
+// the compiler may legally sink read-only loads below the wait.)
+//
+// Shared-memory reads: lane j reads the 32-byte block j of a row as two 16-byte
+// halves, half (j >> 2) & 1 first, so every quarter-warp phase touches 32
+// distinct banks.  The activation words are paired in the same order.
+//
+//  * ffn_up_kernel: RMSNorm + Q8_0 quantization of x (every CTA, from L2),
+//    stacked gate|up block dots, SiLU(g)*u, and Q8_0 quantization of each
+//    32-output block of h (a CTA owns whole blocks), so the down projection
+//    reads codes directly.
+//  * gemv_prefetch_kernel: batch-1 Q8_0 GEMV over pre-quantized input with the
+//    NONE or RESIDUAL epilogue (the down projection, and small GEMVs).
+#include <mutex>
+
+#include "qg_common.cuh"
+#include "qg_norm.cuh"
+
+namespace qg {
+
+// ---------------------------------------------------------------------------
+// shared pieces
+// ---------------------------------------------------------------------------
+
+// S * (d_w * d_x) accumulated the same way as the streaming GEMV kernels.
+__device__ __forceinline__ float block_term(const u32x8 &w, const u32x8 &x, float dw, float dx, float acc)
+{
+    int s = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s = dp4a(w.v[i], x.v[i], s);
+    return fmaf(small_int_to_float(s), dw * dx, acc);
+}
+
+__device__ __forceinline__ void zero(u32x8 &w)
+{
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w.v[i] = 0u;
+}
+
+// 32-byte block at p (16-byte aligned), half c0 first.
+__device__ __forceinline__ u32x8 ld_block_halves(const int8_t *p, int c0)
+{
+    const uint4 a = *reinterpret_cast<const uint4 *>(p + 16 * c0);
+    const uint4 b = *reinterpret_cast<const uint4 *>(p + 16 * (c0 ^ 1));
+    u32x8 r;
+    r.v[0] = a.x; r.v[1] = a.y; r.v[2] = a.z; r.v[3] = a.w;
+    r.v[4] = b.x; r.v[5] = b.y; r.v[6] = b.z; r.v[7] = b.w;
+    return r;
+}
+
+__device__ __forceinline__ int lane_half(int lane) { return (lane >> 2) & 1; }
+
+// Copy rows [row0, row0 + nrow) of a row-major byte matrix (row_bytes per row,
+// a multiple of 16) into shared memory at dst, 16 bytes per cp.async.
+__device__ __forceinline__ void stage_rows(uint8_t *dst, const void *src, int64_t row0, int nrow, int row_bytes)
+{
+    const int per_row = row_bytes >> 4;
+    const int total = nrow * per_row;
+    const uint8_t *g = static_cast<const uint8_t *>(src) + row0 * row_bytes;
+    for (int c = threadIdx.x; c < total; c += blockDim.x) {
+        const int r = c / per_row, cc = c - r * per_row;
+        cp_async_16(smem_addr(dst + r * row_bytes + cc * 16), g + static_cast<int64_t>(r) * row_bytes + cc * 16);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// gate|up with the norm in front and SiLU + quantization behind
+// ---------------------------------------------------------------------------
+struct FfnUpParams {
+    const float *x;       // [k] input row (written by the previous kernel)
+    const float *gamma;   // [k]
+    const int8_t *w_qs;   // stacked [2F][k]
+    const uint16_t *w_d;  // [2F][k/32]
+    float *h;             // [F] silu(g) * u
+    int8_t *hq;           // [F] Q8_0 codes of h
+    uint16_t *hd;         // [F/32] binary16 scales of h
+    int8_t *xq_out;       // optional [k]   (written by CTA 0)
+    uint16_t *xd_out;     // optional [k/32]
+    float *r_out;         // optional [1]
+    int k;
+    int nb;
+    int64_t half;         // F
+    float eps;
+};
+
+__host__ __device__ constexpr size_t ffn_up_smem_bytes(int k)
+{
+    // values [64][k] | scales [64][k/32] u16 | gamma [k] f32 | x codes [k] | x scales [k/32] f32 | h [32] | scratch
+    return static_cast<size_t>(64) * k + 64 * (k / 32) * 2 + 4 * k + k + 4 * (k / 32) + 4 * 32 + 4 * (2 * 16 + 1);
+}
+
+// One CTA per 32-output block of h (rows o..o+31 of gate and of up).
+// NBL = ceil(k / 1024) blocks per lane; warps = 8 * NBL, each owning 4 / NBL outputs.
+template <int NBL>
+__global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
+{
+    constexpr int OPW = 4 / NBL;
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int K = p.k, nb = p.nb;
+    int8_t *s_w = reinterpret_cast<int8_t *>(smem);
+    uint16_t *s_wd = reinterpret_cast<uint16_t *>(smem + 64 * K);
+    float *s_gamma = reinterpret_cast<float *>(smem + 64 * K + 128 * nb);
+    int8_t *s_xq = reinterpret_cast<int8_t *>(s_gamma + K);
+    float *s_xd = reinterpret_cast<float *>(s_xq + K);
+    float *s_h = s_xd + nb;
+    float *s_scratch = s_h + 32;
+
+    const int t = threadIdx.x;
+    const int lane = t & 31;
+    const int warp = t >> 5;
+    const int64_t ob = static_cast<int64_t>(blockIdx.x) * 32;
+
+    pdl_trigger();
+
+    // ---- stage everything that does not depend on the previous kernel -------
+    stage_rows(reinterpret_cast<uint8_t *>(s_gamma), p.gamma, 0, 1, 4 * K);
+    stage_rows(reinterpret_cast<uint8_t *>(s_wd), p.w_d, ob, 32, 2 * nb);
+    stage_rows(reinterpret_cast<uint8_t *>(s_wd + 32 * nb), p.w_d, p.half + ob, 32, 2 * nb);
+    cp_async_commit();  // group: gain and scales
+    stage_rows(reinterpret_cast<uint8_t *>(s_w), p.w_qs, ob, 32, K);
+    stage_rows(reinterpret_cast<uint8_t *>(s_w + 32 * K), p.w_qs, p.half + ob, 32, K);
+    cp_async_commit();  // group: weight values
+
+    pdl_wait();
+
+    // ---- RMSNorm + Q8_0 quantization of x, in every CTA ----------------------
+    f32pair acc2 = {0.0f, 0.0f};
+    float4 xv4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (4 * t < K) {
+        xv4 = *reinterpret_cast<const float4 *>(p.x + 4 * t);
+        pair_add_square(acc2, xv4.x);
+        pair_add_square(acc2, xv4.y);
+        pair_add_square(acc2, xv4.z);
+        pair_add_square(acc2, xv4.w);
+    }
+    cp_async_wait<1>();  // this thread's gain / scale copies
+    const float r = block_rms_inv(acc2, K, p.eps, s_scratch);  // (synchronises the block)
+    {
+        const int b = t >> 3, sub = t & 7;  // eight lanes per 32-value block
+        const bool live = b < nb;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (live) {
+            const float4 g = *reinterpret_cast<const float4 *>(s_gamma + 4 * t);
+            v.x = __fmul_rn(__fmul_rn(xv4.x, r), g.x);
+            v.y = __fmul_rn(__fmul_rn(xv4.y, r), g.y);
+            v.z = __fmul_rn(__fmul_rn(xv4.z, r), g.z);
+            v.w = __fmul_rn(__fmul_rn(xv4.w, r), g.w);
+        }
+        float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        if (live) {
+            const float dd = __fdiv_rn(m, 127.0f);
+            const uint32_t c = (static_cast<uint32_t>(q8_code(v.x, dd)) & 0xffu) |
+                               ((static_cast<uint32_t>(q8_code(v.y, dd)) & 0xffu) << 8) |
+                               ((static_cast<uint32_t>(q8_code(v.z, dd)) & 0xffu) << 16) |
+                               ((static_cast<uint32_t>(q8_code(v.w, dd)) & 0xffu) << 24);
+            reinterpret_cast<uint32_t *>(s_xq)[t] = c;
+            const uint16_t dbits = f2h_rn(dd);
+            if (sub == 0) s_xd[b] = h2f(dbits);
+            if (blockIdx.x == 0) {
+                if (p.xq_out) reinterpret_cast<uint32_t *>(p.xq_out)[t] = c;
+                if (p.xd_out && sub == 0) p.xd_out[b] = dbits;
+            }
+        }
+        if (blockIdx.x == 0 && t == 0 && p.r_out) *p.r_out = r;
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+
+    const int c0 = lane_half(lane);
+    u32x8 xv[NBL];
+    float xs[NBL];
+#pragma unroll
+    for (int j = 0; j < NBL; ++j) {
+        const int blk = lane + 32 * j;
+        if (blk < nb) {
+            xv[j] = ld_block_halves(s_xq + blk * QK, c0);
+            xs[j] = s_xd[blk];
+        } else {
+            zero(xv[j]);
+            xs[j] = 0.0f;
+        }
+    }
+
+    // ---- block dots, SiLU(g) * u --------------------------------------------
+#pragma unroll
+    for (int i = 0; i < OPW; ++i) {
+        const int rg = warp * OPW + i;  // gate row within the slab; up row = rg + 32
+        float g = 0.0f, u = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NBL; ++j) {
+            const int blk = lane + 32 * j;
+            if (blk < nb) {
+                g = block_term(ld_block_halves(s_w + rg * K + blk * QK, c0), xv[j], h2f(s_wd[rg * nb + blk]), xs[j], g);
+                u = block_term(ld_block_halves(s_w + (rg + 32) * K + blk * QK, c0), xv[j],
+                               h2f(s_wd[(rg + 32) * nb + blk]), xs[j], u);
+            }
+        }
+        g = warp_sum(g);
+        u = warp_sum(u);
+        if (lane == 0) {
+            const float hv = silu_mul(g, u);
+            s_h[rg] = hv;
+            p.h[ob + rg] = hv;
+        }
+    }
+    __syncthreads();
+
+    // ---- Q8_0 quantization of this CTA's 32-value block of h -----------------
+    if (warp == 0) {
+        const float v = s_h[lane];
+        const float m = warp_max(fabsf(v));
+        const float dd = __fdiv_rn(m, 127.0f);
+        p.hq[ob + lane] = static_cast<int8_t>(q8_code(v, dd));
+        if (lane == 0) p.hd[blockIdx.x] = f2h_rn(dd);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// batch-1 GEMV with the whole weight slab staged before the wait
+// ---------------------------------------------------------------------------
+struct PrefetchParams {
+    const int8_t *w_qs;
+    const uint16_t *w_d;
+    const int8_t *xq;
+    const uint16_t *xd;
+    const float *residual;  // RESIDUAL epilogue (may equal y)
+    float *y;
+    int64_t n_rows;
+    int k;
+    int nb;
+    int epi;
+    int rows_per_cta;
+};
+
+// CTA c owns rows [c * rows_per_cta, ...); warp w computes rows w, w + W, ...
+template <int NBL>
+__global__ void __launch_bounds__(256) gemv_prefetch_kernel(const PrefetchParams p)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int K = p.k, nb = p.nb, R = p.rows_per_cta;
+    int8_t *s_w = reinterpret_cast<int8_t *>(smem);
+    uint16_t *s_wd = reinterpret_cast<uint16_t *>(smem + static_cast<size_t>(R) * K);
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nw = blockDim.x >> 5;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * R;
+    const int nrow = static_cast<int>(p.n_rows - r0 < R ? p.n_rows - r0 : R);
+
+    pdl_trigger();
+    stage_rows(reinterpret_cast<uint8_t *>(s_w), p.w_qs, r0, nrow, K);
+    stage_rows(reinterpret_cast<uint8_t *>(s_wd), p.w_d, r0, nrow, 2 * nb);
+    cp_async_commit();
+
+    pdl_wait();
+
+    const int c0 = lane_half(lane);
+    u32x8 xv[NBL];
+    float xs[NBL];
+#pragma unroll
+    for (int j = 0; j < NBL; ++j) {
+        const int blk = lane + 32 * j;
+        if (blk < nb) {
+            xv[j] = ld_block_halves(p.xq + blk * QK, c0);
+            xs[j] = h2f(p.xd[blk]);
+        } else {
+            zero(xv[j]);
+            xs[j] = 0.0f;
+        }
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+
+    for (int rr = warp; rr < nrow; rr += nw) {
+        float acc = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NBL; ++j) {
+            const int blk = lane + 32 * j;
+            if (blk < nb)
+                acc = block_term(ld_block_halves(s_w + rr * K + blk * QK, c0), xv[j], h2f(s_wd[rr * nb + blk]), xs[j],
+                                 acc);
+        }
+        acc = warp_sum(acc);
+        if (lane == 0) {
+            const int64_t row = r0 + rr;
+            p.y[row] = (p.epi == QG_EPI_RESIDUAL_ADD) ? p.residual[row] + acc : acc;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+constexpr size_t kMaxSmem = 220 * 1024;
+
+// The staged copies move 16-byte pieces of whole rows: rows of scales must be
+// a multiple of 16 bytes, i.e. k a multiple of 256.
+bool ffn_up_supported(int64_t k, int64_t half)
+{
+    return k % 256 == 0 && k <= 2048 && half % 32 == 0 && ffn_up_smem_bytes(static_cast<int>(k)) <= kMaxSmem;
+}
+
+template <int NBL>
+static cudaError_t ffn_up_attr()
+{
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        err = cudaFuncSetAttribute(ffn_up_kernel<NBL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(kMaxSmem));
+    });
+    return err;
+}
+
+cudaError_t launch_ffn_up(const float *x, const float *gamma, int64_t k, float eps, const int8_t *w_qs,
+                          const uint16_t *w_d, int64_t half, float *h, int8_t *hq, uint16_t *hd, int8_t *xq_out,
+                          uint16_t *xd_out, float *r_out, cudaStream_t s)
+{
+    if (half == 0) return cudaSuccess;
+    FfnUpParams p;
+    p.x = x;
+    p.gamma = gamma;
+    p.w_qs = w_qs;
+    p.w_d = w_d;
+    p.h = h;
+    p.hq = hq;
+    p.hd = hd;
+    p.xq_out = xq_out;
+    p.xd_out = xd_out;
+    p.r_out = r_out;
+    p.k = static_cast<int>(k);
+    p.nb = static_cast<int>(k / QK);
+    p.half = half;
+    p.eps = eps;
+    const dim3 grid(static_cast<unsigned>(half / 32));
+    const size_t smem = ffn_up_smem_bytes(p.k);
+    if (k <= 1024) {
+        if (cudaError_t e = ffn_up_attr<1>(); e != cudaSuccess) return e;
+        return launch_pdl(ffn_up_kernel<1>, grid, dim3(256), smem, s, p);
+    }
+    if (cudaError_t e = ffn_up_attr<2>(); e != cudaSuccess) return e;
+    return launch_pdl(ffn_up_kernel<2>, grid, dim3(512), smem, s, p);
+}
+
+// Rows per CTA when the rows are spread over one wave of num_sms CTAs.
+static int64_t prefetch_rows_per_cta(int64_t n_rows)
+{
+    const int64_t sms = num_sms();
+    return (n_rows + sms - 1) / sms;
+}
+
+bool prefetch_supported(int64_t n_rows, int64_t k)
+{
+    if (k % 256 != 0 || k > 4096 || n_rows <= 0) return false;
+    const int64_t rpc = prefetch_rows_per_cta(n_rows);
+    return static_cast<size_t>(rpc * (k + k / 16)) <= 160 * 1024;
+}
+
+template <int NBL>
+static cudaError_t prefetch_attr()
+{
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        err = cudaFuncSetAttribute(gemv_prefetch_kernel<NBL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(kMaxSmem));
+    });
+    return err;
+}
+
+template <int NBL>
+static cudaError_t launch_prefetch_nbl(PrefetchParams p, cudaStream_t s)
+{
+    if (cudaError_t e = prefetch_attr<NBL>(); e != cudaSuccess) return e;
+    const int64_t rpc = prefetch_rows_per_cta(p.n_rows);
+    p.rows_per_cta = static_cast<int>(rpc);
+    const dim3 grid(static_cast<unsigned>((p.n_rows + rpc - 1) / rpc));
+    const dim3 block(static_cast<unsigned>(32 * (rpc < 8 ? rpc : 8)));
+    const size_t smem = static_cast<size_t>(rpc) * (p.k + 2 * p.nb);
+    return launch_pdl(gemv_prefetch_kernel<NBL>, grid, block, smem, s, p);
+}
+
+cudaError_t launch_gemv_prefetch(const int8_t *w_qs, const uint16_t *w_d, int64_t n_rows, int64_t k,
+                                 const int8_t *xq, const uint16_t *xd, int epi, const float *residual, float *y,
+                                 cudaStream_t s)
+{
+    if (n_rows == 0) return cudaSuccess;
+    PrefetchParams p;
+    p.w_qs = w_qs;
+    p.w_d = w_d;
+    p.xq = xq;
+    p.xd = xd;
+    p.residual = residual;
+    p.y = y;
+    p.n_rows = n_rows;
+    p.k = static_cast<int>(k);
+    p.nb = static_cast<int>(k / QK);
+    p.epi = epi;
+    p.rows_per_cta = 0;
+    switch ((p.nb + 31) / 32) {
+    case 1: return launch_prefetch_nbl<1>(p, s);
+    case 2: return launch_prefetch_nbl<2>(p, s);
+    case 3: return launch_prefetch_nbl<3>(p, s);
+    case 4: return launch_prefetch_nbl<4>(p, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace qg

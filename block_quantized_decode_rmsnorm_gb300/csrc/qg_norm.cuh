@@ -1,15 +1,21 @@
-// RMSNorm statistic on the GPU: r = 1 / sqrt(mean(x^2) + eps), evaluated as in
-// f64 and rounded once to f32.
+// RMSNorm statistic on the GPU: r = 1 / sqrt(mean(x^2) + eps) rounded to f32,
+// agreeing with an f64 evaluation of the same expression.
 //
-// GB300 runs f64 at a small fraction of its f32 rate, so a block-wide f64 sum
-// would cost microseconds per CTA.  Instead each thread forms the exact square
-// x*x = p + e (p = fl(x*x), e = fma(x, x, -p), Dekker's product) and adds both
-// parts into a compensated pair (hi, lo) with Knuth's error-free two-sum; pairs
-// are combined across the warp the same way and the per-warp pairs are added in
-// f64 by one thread.  The sum carries about 48 significant bits, so r after the
-// final f64 sqrt, division and rounding to f32 equals the f64-evaluated value
-// except when that value lies within ~2^-40 (relative) of an f32 rounding
-// boundary.
+// GB300 runs f64 at a small fraction of its f32 rate (and f64 division and
+// square root are long dependent chains), so everything here is f32 with
+// error-free transformations:
+//  * each thread forms the exact square x*x = p + e (p = fl(x*x),
+//    e = fma(x, x, -p); Dekker's product) and adds both parts into a
+//    compensated pair (hi, lo) with Knuth's two-sum; pairs are merged across the
+//    warp and the block the same way;
+//  * mean = s / k as a pair (the division's remainder is exact through an FMA),
+//    plus eps with a two-sum;
+//  * y0 = rsqrtf(a), then one Newton-Taylor step r = y0 (1 + e/2 + 3e^2/8) with
+//    the residual e = 1 - a y0^2 evaluated from exact products, and one final
+//    f32 rounding.
+// The result is within ~2^-46 (relative) of the real value before that final
+// rounding, so it equals the f64-evaluated r except when the real value lies
+// that close to a midpoint between two f32 numbers.
 #pragma once
 
 #include "qg_common.cuh"
@@ -67,8 +73,36 @@ __device__ __forceinline__ f32pair warp_pair_sum(f32pair v)
     return v;
 }
 
+// r from the pair sum of squares (one thread).
+__device__ __forceinline__ float rms_inv_from_pair(f32pair s, int k, float eps)
+{
+    const float kf = static_cast<float>(k);  // exact: k < 2^24
+    const float m_hi = __fdiv_rn(s.hi, kf);
+    const float rem = __fmaf_rn(-m_hi, kf, s.hi);  // s.hi - m_hi * k, exact
+    const float m_lo = __fdiv_rn(__fadd_rn(rem, s.lo), kf);
+    float a_hi, a_e;
+    two_sum(m_hi, eps, a_hi, a_e);
+    float a_lo = __fadd_rn(a_e, m_lo);
+    const float t = __fadd_rn(a_hi, a_lo);  // renormalise, |a_hi| >= |a_lo|
+    a_lo = __fsub_rn(a_lo, __fsub_rn(t, a_hi));
+    a_hi = t;
+    if (a_hi == 0.0f) return __int_as_float(0x7f800000);  // 1/sqrt(0)
+    if (isinf(a_hi)) return 0.0f;
+    const float y0 = rsqrtf(a_hi);
+    const float p = __fmul_rn(y0, y0);
+    const float pe = __fmaf_rn(y0, y0, -p);        // y0^2 = p + pe
+    const float th = __fmul_rn(a_hi, p);
+    const float te = __fmaf_rn(a_hi, p, -th);      // a_hi p = th + te
+    float e = __fsub_rn(1.0f, th);                 // exact: th is within [0.5, 2]
+    e = __fsub_rn(e, te);
+    e = __fmaf_rn(-a_hi, pe, e);
+    e = __fmaf_rn(-a_lo, p, e);                    // e = 1 - a y0^2 (to ~2^-46)
+    const float corr = __fmul_rn(y0, __fmul_rn(e, __fmaf_rn(0.375f, e, 0.5f)));
+    return __fadd_rn(y0, corr);
+}
+
 // Block-wide: every thread passes its pair; returns r to every thread.
-// `scratch` holds 2 * (blockDim.x / 32) floats + 1; all threads must call.
+// `scratch` holds 2 * (blockDim.x / 32) + 1 floats; all threads must call.
 __device__ __forceinline__ float block_rms_inv(f32pair v, int k, float eps, float *scratch)
 {
     v = warp_pair_sum(v);
@@ -80,11 +114,9 @@ __device__ __forceinline__ float block_rms_inv(f32pair v, int k, float eps, floa
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        double t = 0.0;
-        for (int w = 0; w < nw; ++w) t += static_cast<double>(scratch[2 * w]);
-        for (int w = 0; w < nw; ++w) t += static_cast<double>(scratch[2 * w + 1]);
-        const double mean = t / static_cast<double>(k);
-        scratch[2 * nw] = static_cast<float>(1.0 / sqrt(mean + static_cast<double>(eps)));
+        f32pair t = {scratch[0], scratch[1]};
+        for (int w = 1; w < nw; ++w) t = pair_merge(t, f32pair{scratch[2 * w], scratch[2 * w + 1]});
+        scratch[2 * nw] = rms_inv_from_pair(t, k, eps);
     }
     __syncthreads();
     return scratch[2 * nw];

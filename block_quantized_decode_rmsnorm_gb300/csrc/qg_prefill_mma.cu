@@ -24,19 +24,14 @@ constexpr int PF_THREADS = 256;
 constexpr int PF_STAGES = 4;
 constexpr int PF_MAX_NB = 256;  // K <= 8192
 
-__device__ __forceinline__ uint32_t smem_u32(const void *p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return smem_addr(p); }
 
+// 16-byte async copy that zero-fills instead of reading when !valid (rows past the end).
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, bool valid)
 {
-    const int n = valid ? 16 : 0;  // zero-fill rows past the end
+    const int n = valid ? 16 : 0;
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
 {

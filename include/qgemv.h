@@ -169,6 +169,42 @@ QG_API qg_status qgemm_q8_0_prefill(const int8_t *w_qs, const uint16_t *w_d, int
                              float *y, qg_stream_t stream);
 
 /*
+ * qg_ffn_up_q8_0 - the first half of a decode feed-forward block in one launch:
+ * RMSNorm of x, Q8_0 quantization of x_hat, the stacked gate|up product, and
+ * SiLU(g) * u, whose 32-value blocks are quantized to Q8_0 on the way out.
+ * [Phobos] Fast Decode (quantize once and share; stack projections that read
+ * the same input); [Herbert] Emitting for a GPU (normalization fused with the
+ * projection that follows it, activation fused with the projection before it).
+ *   Arithmetic identical to rmsnorm_quantize -> qgemv_q8_0(SILU_MUL_HALVES)
+ *   -> quantize_act_q8_0, bit for bit.
+ *   x: device f32[hidden] (read); gamma: device f32[hidden] (read)
+ *   w_qs, w_d: stacked gate|up weight planes [2*ffn][hidden], [2*ffn][hidden/32]
+ *   h: device f32[ffn] (written); hq: int8[ffn], hd: binary16 bits [ffn/32] (written)
+ *   xq_out, xd_out, inv_rms_out: optional copies of the quantized input and of r
+ *   hidden % 256 == 0 and hidden <= 2048; ffn % 32 == 0 (else QG_ERR_UNSUPPORTED
+ *   or QG_ERR_SHAPE); w_d 16-byte aligned.
+ */
+QG_API qg_status qg_ffn_up_q8_0(const float *x, const float *gamma, int64_t hidden, float eps,
+                                const int8_t *w_qs, const uint16_t *w_d, int64_t ffn,
+                                float *h, int8_t *hq, uint16_t *hd, int8_t *xq_out,
+                                uint16_t *xd_out, float *inv_rms_out, qg_stream_t stream);
+
+/*
+ * qg_decode_ffn_q8_0 - one decode feed-forward block, x <- x + down(h), in two
+ * launches: qg_ffn_up_q8_0, then qgemv_q8_0(down, hq, hd, QG_EPI_RESIDUAL_ADD)
+ * in place on x ([Phobos] Fast Decode: fold the residual add into the matmul).
+ *   x: device f32[hidden], read and overwritten with the block's output
+ *   wgu_*: stacked gate|up planes [2*ffn][hidden]; wdn_*: down planes [hidden][ffn]
+ *   h, hq, hd: caller-owned work buffers f32[ffn], int8[ffn], binary16[ffn/32]
+ *              (left holding this block's activation); hq 32-byte aligned
+ *   shapes as qg_ffn_up_q8_0; both scale planes 16-byte aligned.
+ */
+QG_API qg_status qg_decode_ffn_q8_0(float *x, const float *gamma, int64_t hidden, int64_t ffn,
+                                    float eps, const int8_t *wgu_qs, const uint16_t *wgu_d,
+                                    const int8_t *wdn_qs, const uint16_t *wdn_d, float *h,
+                                    int8_t *hq, uint16_t *hd, qg_stream_t stream);
+
+/*
  * qg_debug_block_dots_q8_0 - the exact per-block int32 sums, for parity checks.
  *   s[b][n][j] = sum_{i<32} w_qs[n][32j+i] * xq[b][32j+i]   (int32, exact)
  *   s: device int32[batch][n_rows][k/32] (written); batch <= 8.

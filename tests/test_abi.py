@@ -98,3 +98,20 @@ def test_binding_refuses_cpu_tensors():
 
     with pytest.raises(ValueError, match="CUDA"):
         api.quantize_act_q8_0(torch.zeros(1, 32))
+
+
+def test_fused_ffn_argument_errors(lib):
+    f = lib.qg_ffn_up_q8_0
+    eps = ctypes.c_float(1e-6)
+    # hidden must be a multiple of 256 and at most 2048 for the one-launch path
+    assert f(FAKE, FAKE, 992, eps, FAKE, FAKE, 64, FAKE, FAKE, FAKE, None, None, None, None) == 4
+    assert f(FAKE, FAKE, 4096, eps, FAKE, FAKE, 64, FAKE, FAKE, FAKE, None, None, None, None) == 4
+    # ffn must be a multiple of 32
+    assert f(FAKE, FAKE, 1024, eps, FAKE, FAKE, 48, FAKE, FAKE, FAKE, None, None, None, None) == 3
+    # the weight scale plane must be 16-byte aligned (it is staged in 16-byte pieces)
+    assert f(FAKE, FAKE, 1024, eps, FAKE, FAKE + 2, 64, FAKE, FAKE, FAKE, None, None, None, None) == 2
+    assert f(FAKE, None, 1024, eps, FAKE, FAKE, 64, FAKE, FAKE, FAKE, None, None, None, None) == 1
+    d = lib.qg_decode_ffn_q8_0
+    assert d(FAKE, FAKE, 1024, 3584, eps, FAKE, FAKE, FAKE, FAKE + 2, FAKE, FAKE, FAKE, None) == 2
+    assert d(FAKE, FAKE, 1024, 3584, eps, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 16, FAKE, None) == 2
+    assert d(FAKE, FAKE, 1024, 0, eps, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == 3

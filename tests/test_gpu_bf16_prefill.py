@@ -50,7 +50,7 @@ def test_bf16_gemv(torch, orc, n, k, norm, epi):
     if epi == "silu_mul":
         F = n // 2
         g, u = y64[:F], y64[F:]
-        assert_close(y, orc.silu_mul(g, u), silu_scale(g, u, a64[:F], a64[F:]), TOL_BF16, "bf16 silu")
+        assert_close(y, orc.silu_mul(g, u), silu_scale(g, u, a64[:F], a64[F:], TOL_BF16), TOL_BF16, "bf16 silu")
     elif epi == "residual":
         exact = res.astype(np.float64) + y64
         assert_close(y, exact, a64 + np.abs(res) + np.abs(exact), TOL_BF16, "bf16 residual")

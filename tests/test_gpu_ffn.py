@@ -72,7 +72,7 @@ def test_ffn_staged_parity(torch, orc):
 
     # independent end to end: the oracle from the same x
     ref = orc.decode_ffn(case["x"], case["gamma"], EPS, case["gu_qs"], case["gu_d"], case["dn_qs"], case["dn_d"])
-    flips = int(np.count_nonzero(_snapshot(buf)["hq"] != ref["hq"][0]))
+    flips = int(np.count_nonzero(_snapshot(buf)["hq"] != ref["hq"].ravel()))
     e = norm_err(x.cpu().numpy(), ref["out64"], ref["a_y"] + np.abs(case["x"]) + np.abs(ref["out64"]))
     assert flips <= 8, flips
     assert e.max() <= 1e-4, e.max()
@@ -125,3 +125,109 @@ def test_ffn_layer_chain_parity(torch, orc):
     outs = inputs[1:] + [x.cpu().numpy()]
     for l in range(n_layers):
         check_layer_staged(orc, cases[l], inputs[l], _snapshot(bufs[l]), outs[l], cases[l]["gamma"])
+
+
+# ---------------------------------------------------------------------------
+# fused two-launch path: qg_ffn_up_q8_0 + qgemv_q8_0(down, residual)
+# ---------------------------------------------------------------------------
+
+def test_fused_up_bit_identical_to_composition_and_oracle(torch, orc):
+    """One launch of qg_ffn_up_q8_0 gives the same bits as rmsnorm_quantize ->
+    qgemv_q8_0(silu_mul) -> quantize_act_q8_0, and passes the staged oracle checks."""
+    from block_quantized_decode_rmsnorm_gb300 import api
+
+    case = synth.ffn_case(2)
+    layer = _layer(torch, case)
+    x = to_dev(case["x"], torch)
+    xq = torch.empty((HIDDEN,), dtype=torch.int8, device="cuda")
+    xd = torch.empty((HIDDEN // 32,), dtype=torch.float16, device="cuda")
+    r = torch.empty((1,), dtype=torch.float32, device="cuda")
+    h, hq, hd = api.qg_ffn_up_q8_0(x, layer.gamma, layer.gate_up, EPS, xq_out=xq, xd_out=xd, inv_rms_out=r)
+    buf = api.FFNBuffers.allocate(HIDDEN, FFN, "cuda")
+    x2 = x.clone()
+    api.decode_ffn_q8_0(x2, layer, buf, EPS)
+    torch.cuda.synchronize()
+    assert np.array_equal(xq.cpu().numpy(), buf.xq[0].cpu().numpy())
+    assert np.array_equal(f16_to_np_bits(xd), f16_to_np_bits(buf.xd)[0])
+    assert np.array_equal(h.cpu().numpy(), buf.h[0].cpu().numpy())
+    assert np.array_equal(hq.cpu().numpy(), buf.hq[0].cpu().numpy())
+    assert np.array_equal(f16_to_np_bits(hd), f16_to_np_bits(buf.hd)[0])
+    _, _, r_o, _ = orc.rmsnorm_quantize(case["x"], case["gamma"], EPS)
+    assert r.item() == r_o
+
+
+def test_fused_decode_ffn_matches_unfused_and_oracle(torch, orc):
+    from block_quantized_decode_rmsnorm_gb300 import api
+
+    n_layers = 3
+    cases = [synth.ffn_case(5, layer=l) for l in range(n_layers)]
+    layers = [_layer(torch, c) for c in cases]
+    buf_f = api.FFNBuffers.allocate(HIDDEN, FFN, "cuda")
+    buf_u = api.FFNBuffers.allocate(HIDDEN, FFN, "cuda")
+    xf = to_dev(cases[0]["x"], torch)
+    xu = xf.clone()
+    for l in range(n_layers):
+        x_in = xf.cpu().numpy().copy()
+        api.qg_decode_ffn_q8_0(xf, layers[l], buf_f, EPS)
+        api.decode_ffn_q8_0(xu, layers[l], buf_u, EPS)
+        torch.cuda.synchronize()
+        assert np.array_equal(xf.cpu().numpy(), xu.cpu().numpy()), f"layer {l}"
+        snap = _snapshot(buf_u)
+        check_layer_staged(orc, cases[l], x_in, snap, xf.cpu().numpy(), cases[l]["gamma"])
+
+
+def test_fused_graph_replay(torch, orc):
+    from block_quantized_decode_rmsnorm_gb300 import api
+
+    case = synth.ffn_case(6)
+    layer = _layer(torch, case)
+    buf = api.FFNBuffers.allocate(HIDDEN, FFN, "cuda")
+    x0 = to_dev(case["x"], torch)
+    x = x0.clone()
+    api.qg_decode_ffn_q8_0(x, layer, buf, EPS)
+    torch.cuda.synchronize()
+    eager = x.cpu().numpy()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    xg = x0.clone()
+    with torch.cuda.stream(s):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(4):  # four layers sharing weights: exercises back-to-back PDL edges
+                api.qg_decode_ffn_q8_0(xg, layer, buf, EPS, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    ref = x0.clone()
+    for _ in range(4):
+        api.qg_decode_ffn_q8_0(ref, layer, buf, EPS)
+    torch.cuda.synchronize()
+    want = ref.cpu().numpy()
+    for _ in range(3):
+        xg.copy_(x0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(xg.cpu().numpy(), want)
+    assert not np.array_equal(want, eager)
+
+
+@pytest.mark.parametrize("hidden,ffn", [(256, 96), (2048, 1024), (768, 64)])
+def test_fused_other_shapes(torch, orc, hidden, ffn):
+    from block_quantized_decode_rmsnorm_gb300 import api
+
+    case = synth.ffn_case(7, hidden=hidden, ffn=ffn)
+    layer = _layer(torch, case)
+    buf = api.FFNBuffers.allocate(hidden, ffn, "cuda")
+    x = to_dev(case["x"], torch)
+    h, hq, hd = api.qg_ffn_up_q8_0(x, layer.gamma, layer.gate_up, EPS)
+    torch.cuda.synchronize()
+    q, d, r, _ = orc.rmsnorm_quantize(case["x"], case["gamma"], EPS)
+    gu, a_gu = orc.gemv_q8_0(case["gu_qs"], case["gu_d"], q, d)
+    g, u = gu[0, :ffn], gu[0, ffn:]
+    assert_close(h.cpu().numpy(), orc.silu_mul(g, u), silu_scale(g, u, a_gu[0, :ffn], a_gu[0, ffn:]), TOL_Q8, "h")
+    oq, od = orc.quantize_q8_0(h.cpu().numpy()[None, :])
+    assert np.array_equal(hq.cpu().numpy(), oq[0]) and np.array_equal(f16_to_np_bits(hd), od[0])
+    x_in = case["x"].copy()
+    api.qg_decode_ffn_q8_0(x, layer, buf, EPS)
+    torch.cuda.synchronize()
+    y, a_y = orc.gemv_q8_0(case["dn_qs"], case["dn_d"], buf.hq.cpu().numpy(), f16_to_np_bits(buf.hd))
+    exact = x_in.astype(np.float64) + y[0]
+    assert_close(x.cpu().numpy(), exact, a_y[0] + np.abs(x_in) + np.abs(exact), TOL_Q8, "out")
