@@ -45,6 +45,36 @@ __device__ __forceinline__ u32x8 ld_stream_32B(const void *p)
     return r;
 }
 
+// L2 policy for data read once per step (weights): evict first, so that the
+// small activations, gains and scales of the step stay resident in L2.
+__device__ __forceinline__ uint64_t l2_evict_first_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// L2 policy for small data read every step (gains): keep it resident.
+__device__ __forceinline__ uint64_t l2_evict_last_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// As ld_stream_32B, with an L2 cache policy.
+__device__ __forceinline__ u32x8 ld_stream_32B(const void *p, uint64_t pol)
+{
+    u32x8 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.L2::256B.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+                 : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3]), "=r"(r.v[4]), "=r"(r.v[5]),
+                   "=r"(r.v[6]), "=r"(r.v[7])
+                 : "l"(p), "l"(pol));
+    return r;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
 // 16 bytes through the read-only path.  p must be 16-byte aligned.
 __device__ __forceinline__ uint4 ld_nc_16B(const void *p)
 {
@@ -106,13 +136,43 @@ __device__ __forceinline__ double warp_sum_f64(double v)
 }
 
 // Q8_0 code of one value given the block's f32 scale d: round half away from
-// zero of v / d (IEEE division), clamped to [-127, 127]; 0 when d == 0.
-__device__ __forceinline__ int q8_code(float v, float d)
+// zero of fl(v / d) (the IEEE-rounded quotient), clamped to [-127, 127]; 0 when
+// d == 0.
+//
+// rd = __frcp_rn(d).  t = fl(v * rd) is within 2.5 ulp of fl(v / d), so the two
+// round to the same integer unless a half-integer lies within 4 ulp of t; only
+// then (or when rd overflowed) is the exact quotient computed.  The result is
+// therefore always that of round(fl(v / d)).
+__device__ __forceinline__ int q8_code(float v, float d, float rd)
 {
     if (d == 0.0f) return 0;
-    float t = roundf(__fdiv_rn(v, d));
+    float t = __fmul_rn(v, rd);
+    const float a = fabsf(t);
+    const float frac = a - floorf(a);  // exact for a < 2^23
+    if (!(fabsf(frac - 0.5f) > a * 0x1p-20f) || !(a < 1e30f)) t = __fdiv_rn(v, d);
+    t = roundf(t);
     t = fminf(fmaxf(t, -127.0f), 127.0f);
     return static_cast<int>(t);
+}
+
+// fl(m / 127) without a division: q0 = fl(m c), c = fl(1/127), then one FMA
+// correction.  Equal to the IEEE quotient for every finite non-negative f32 m
+// (checked exhaustively over all 2^31 - 2^23 such values against m / 127.0f).
+__device__ __forceinline__ float div127(float m)
+{
+    constexpr float c = 1.0f / 127.0f;
+    const float q0 = __fmul_rn(m, c);
+    const float r = __fmaf_rn(-q0, 127.0f, m);
+    return __fmaf_rn(r, c, q0);
+}
+
+// The four codes of v as one little-endian word.
+__device__ __forceinline__ uint32_t q8_pack4(float4 v, float d, float rd)
+{
+    return (static_cast<uint32_t>(q8_code(v.x, d, rd)) & 0xffu) |
+           ((static_cast<uint32_t>(q8_code(v.y, d, rd)) & 0xffu) << 8) |
+           ((static_cast<uint32_t>(q8_code(v.z, d, rd)) & 0xffu) << 16) |
+           ((static_cast<uint32_t>(q8_code(v.w, d, rd)) & 0xffu) << 24);
 }
 
 // silu(g) * u with silu(g) = g / (1 + e^-g).  For g < 0 the same value is
@@ -135,6 +195,11 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void *src)
 {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
 }
+__device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void *src, uint64_t pol)
+{
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src), "l"(pol)
+                 : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
@@ -142,6 +207,62 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+
+// ---------------------------------------------------------------------------
+// Bulk (TMA) copies global -> shared with mbarrier completion
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// One bulk copy of `bytes` (multiple of 16; both addresses 16-byte aligned).
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                              uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{ .reg .pred q; mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2; selp.u32 %0, 1, 0, q; }"
+                 : "=r"(ok)
+                 : "r"(smem_addr(bar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity`; false if it has not completed within limit_ns.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > limit_ns) return false;
+    return true;
+}
+
+// Limit for a wait on copies that were issued long before: one second.
+constexpr uint64_t kCopyWaitLimitNs = 1000000000ull;
 
 }  // namespace qg
 

@@ -69,17 +69,34 @@ __device__ __forceinline__ u32x8 ld_block_halves(const int8_t *p, int c0)
 
 __device__ __forceinline__ int lane_half(int lane) { return (lane >> 2) & 1; }
 
-// Copy rows [row0, row0 + nrow) of a row-major byte matrix (row_bytes per row,
-// a multiple of 16) into shared memory at dst, 16 bytes per cp.async.
-__device__ __forceinline__ void stage_rows(uint8_t *dst, const void *src, int64_t row0, int nrow, int row_bytes)
+// Sum NV per-lane partials across the warp in one butterfly: at offset 16 a lane
+// keeps half of its values and receives the partner's other half, and so on, so
+// NV values need NV - 1 + (5 - log2 NV) shuffles instead of 5 NV.  Every value
+// is summed over the same lane pairs, in the same order, as warp_sum does.
+// Returns the total of value index  sum over the first log2(NV) offsets o of
+// (lane & o ? NV/2^(step+1) : 0).
+template <int NV>
+__device__ __forceinline__ float warp_sum_many(float (&v)[NV], int lane)
 {
-    const int per_row = row_bytes >> 4;
-    const int total = nrow * per_row;
-    const uint8_t *g = static_cast<const uint8_t *>(src) + row0 * row_bytes;
-    for (int c = threadIdx.x; c < total; c += blockDim.x) {
-        const int r = c / per_row, cc = c - r * per_row;
-        cp_async_16(smem_addr(dst + r * row_bytes + cc * 16), g + static_cast<int64_t>(r) * row_bytes + cc * 16);
+    int n = NV;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        if (n > 1) {
+            const bool upper = (lane & off) != 0;
+#pragma unroll
+            for (int k = 0; k < NV / 2; ++k) {
+                if (k < n / 2) {
+                    const float send = upper ? v[k] : v[k + n / 2];
+                    const float keep = upper ? v[k + n / 2] : v[k];
+                    v[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                }
+            }
+            n /= 2;
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+        }
     }
+    return v[0];
 }
 
 // ---------------------------------------------------------------------------
@@ -99,21 +116,32 @@ struct FfnUpParams {
     int k;
     int nb;
     int64_t half;         // F
+    float inv_k;          // fl(1 / k)
     float eps;
 };
 
 __host__ __device__ constexpr size_t ffn_up_smem_bytes(int k)
 {
-    // values [64][k] | scales [64][k/32] u16 | gamma [k] f32 | x codes [k] | x scales [k/32] f32 | h [32] | scratch
-    return static_cast<size_t>(64) * k + 64 * (k / 32) * 2 + 4 * k + k + 4 * (k / 32) + 4 * 32 + 4 * (2 * 16 + 1);
+    // values [64][k] | scales [64][k/32] u16 | gamma [k] f32 | x codes [k] | x scales [k/32] f32
+    // | h [32] f32 | warp partial pairs [2 * 16] f32
+    return static_cast<size_t>(64) * k + 64 * (k / 32) * 2 + 4 * k + k + 4 * (k / 32) + 4 * 32 + 4 * 32;
 }
 
 // One CTA per 32-output block of h (rows o..o+31 of gate and of up).
 // NBL = ceil(k / 1024) blocks per lane; warps = 8 * NBL, each owning 4 / NBL outputs.
+//
+// After the wait: thread t holds x[4t..4t+3]; the compensated sum of squares
+// is reduced per warp, the warp partials meet in shared memory (one barrier),
+// and every warp merges them with a shuffle tree and evaluates r itself.  Eight
+// threads quantize each 32-value block; the codes go through shared memory to
+// the lanes whose dot products read them (second barrier, which also covers
+// the staged weights).
 template <int NBL>
 __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
 {
-    constexpr int OPW = 4 / NBL;
+    constexpr int OPW = 4 / NBL;  // outputs per warp
+    constexpr int NV = 2 * OPW;   // row sums per warp (gate rows then up rows)
+    constexpr int NW = 8 * NBL;   // warps per CTA
     extern __shared__ __align__(16) uint8_t smem[];
     const int K = p.k, nb = p.nb;
     int8_t *s_w = reinterpret_cast<int8_t *>(smem);
@@ -122,41 +150,100 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
     int8_t *s_xq = reinterpret_cast<int8_t *>(s_gamma + K);
     float *s_xd = reinterpret_cast<float *>(s_xq + K);
     float *s_h = s_xd + nb;
-    float *s_scratch = s_h + 32;
+    float *s_part = s_h + 32;
 
     const int t = threadIdx.x;
     const int lane = t & 31;
     const int warp = t >> 5;
     const int64_t ob = static_cast<int64_t>(blockIdx.x) * 32;
 
+    __shared__ __align__(8) uint64_t s_bar;
     pdl_trigger();
 
     // ---- stage everything that does not depend on the previous kernel -------
-    stage_rows(reinterpret_cast<uint8_t *>(s_gamma), p.gamma, 0, 1, 4 * K);
-    stage_rows(reinterpret_cast<uint8_t *>(s_wd), p.w_d, ob, 32, 2 * nb);
-    stage_rows(reinterpret_cast<uint8_t *>(s_wd + 32 * nb), p.w_d, p.half + ob, 32, 2 * nb);
-    cp_async_commit();  // group: gain and scales
-    stage_rows(reinterpret_cast<uint8_t *>(s_w), p.w_qs, ob, 32, K);
-    stage_rows(reinterpret_cast<uint8_t *>(s_w + 32 * K), p.w_qs, p.half + ob, 32, K);
-    cp_async_commit();  // group: weight values
+    // (bulk copies: one instruction per contiguous slab, completion on s_bar)
+    if (t == 0) mbar_init(&s_bar, 1);
+    __syncthreads();
+    if (t == 0) {
+        const uint64_t pol = l2_evict_first_policy();
+        const uint32_t vbytes = 32u * K, sbytes = 64u * nb;
+        mbar_expect_tx(&s_bar, 4u * K + 2 * sbytes + 2 * vbytes);
+        bulk_copy_g2s(s_gamma, p.gamma, 4u * K, &s_bar, l2_evict_last_policy());
+        bulk_copy_g2s(s_wd, p.w_d + ob * nb, sbytes, &s_bar, pol);
+        bulk_copy_g2s(s_wd + 32 * nb, p.w_d + (p.half + ob) * nb, sbytes, &s_bar, pol);
+        bulk_copy_g2s(s_w, p.w_qs + ob * K, vbytes, &s_bar, pol);
+        bulk_copy_g2s(s_w + 32 * K, p.w_qs + (p.half + ob) * K, vbytes, &s_bar, pol);
+    }
 
     pdl_wait();
 
-    // ---- RMSNorm + Q8_0 quantization of x, in every CTA ----------------------
-    f32pair acc2 = {0.0f, 0.0f};
+    // x first (the one input that comes from the previous kernel) ...
+    const bool live = 4 * t < K;
     float4 xv4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (4 * t < K) {
-        xv4 = *reinterpret_cast<const float4 *>(p.x + 4 * t);
-        pair_add_square(acc2, xv4.x);
-        pair_add_square(acc2, xv4.y);
-        pair_add_square(acc2, xv4.z);
-        pair_add_square(acc2, xv4.w);
+    if (live) xv4 = *reinterpret_cast<const float4 *>(p.x + 4 * t);
+
+    // ... then the staged slab (long since arrived, normally).  A copy that has
+    // not landed within the limit leaves NaN outputs for this block.
+    if (!__syncthreads_and(mbar_wait_bounded(&s_bar, 0, kCopyWaitLimitNs))) {
+        if (warp == 0) {
+            p.h[ob + lane] = __int_as_float(0x7fc00000);
+            p.hq[ob + lane] = 0;
+            if (lane == 0) p.hd[blockIdx.x] = 0x7e00;
+        }
+        mbar_wait_bounded(&s_bar, 0, kCopyWaitLimitNs);
+        return;
     }
-    cp_async_wait<1>();  // this thread's gain / scale copies
-    const float r = block_rms_inv(acc2, K, p.eps, s_scratch);  // (synchronises the block)
+    // While x is in flight, pull this warp's weight rows out of shared memory
+    // into registers (rows: OPW gate rows, then OPW up rows).
+    const int c0 = lane_half(lane);
+    u32x8 wr[NV][NBL];
+    float wsc[NV][NBL];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int row = (i < OPW) ? warp * OPW + i : 32 + warp * OPW + (i - OPW);
+#pragma unroll
+        for (int j = 0; j < NBL; ++j) {
+            const int blk = lane + 32 * j;
+            if (blk < nb) {
+                wr[i][j] = ld_block_halves(s_w + row * K + blk * QK, c0);
+                wsc[i][j] = h2f(s_wd[row * nb + blk]);
+            } else {
+                zero(wr[i][j]);
+                wsc[i][j] = 0.0f;
+            }
+        }
+    }
+
+    // ---- RMSNorm statistic ---------------------------------------------------
+    f32pair acc = {0.0f, 0.0f};
+    if (live) {
+        pair_add_square(acc, xv4.x);
+        pair_add_square(acc, xv4.y);
+        pair_add_square(acc, xv4.z);
+        pair_add_square(acc, xv4.w);
+    }
+    acc = warp_pair_sum(acc);
+    if (lane == 0) {
+        s_part[2 * warp] = acc.hi;
+        s_part[2 * warp + 1] = acc.lo;
+    }
+    __syncthreads();
+    f32pair tot = {0.0f, 0.0f};
+    if (lane < NW) tot = f32pair{s_part[2 * lane], s_part[2 * lane + 1]};
+#pragma unroll
+    for (int off = NW / 2; off >= 1; off >>= 1) {
+        f32pair o;
+        o.hi = __shfl_xor_sync(0xffffffffu, tot.hi, off);
+        o.lo = __shfl_xor_sync(0xffffffffu, tot.lo, off);
+        tot = pair_merge(tot, o);
+    }
+    tot.hi = __shfl_sync(0xffffffffu, tot.hi, 0);
+    tot.lo = __shfl_sync(0xffffffffu, tot.lo, 0);
+    const float r = rms_inv_from_pair(tot, K, p.inv_k, p.eps);
+
+    // ---- Q8_0 quantization of x_hat = (x * r) * gamma, eight threads per block
     {
-        const int b = t >> 3, sub = t & 7;  // eight lanes per 32-value block
-        const bool live = b < nb;
+        const int b = t >> 3, sub = t & 7;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (live) {
             const float4 g = *reinterpret_cast<const float4 *>(s_gamma + 4 * t);
@@ -170,11 +257,8 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
         if (live) {
-            const float dd = __fdiv_rn(m, 127.0f);
-            const uint32_t c = (static_cast<uint32_t>(q8_code(v.x, dd)) & 0xffu) |
-                               ((static_cast<uint32_t>(q8_code(v.y, dd)) & 0xffu) << 8) |
-                               ((static_cast<uint32_t>(q8_code(v.z, dd)) & 0xffu) << 16) |
-                               ((static_cast<uint32_t>(q8_code(v.w, dd)) & 0xffu) << 24);
+            const float dd = div127(m);
+            const uint32_t c = q8_pack4(v, dd, __frcp_rn(dd));
             reinterpret_cast<uint32_t *>(s_xq)[t] = c;
             const uint16_t dbits = f2h_rn(dd);
             if (sub == 0) s_xd[b] = h2f(dbits);
@@ -185,10 +269,8 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
         }
         if (blockIdx.x == 0 && t == 0 && p.r_out) *p.r_out = r;
     }
-    cp_async_wait<0>();
     __syncthreads();
 
-    const int c0 = lane_half(lane);
     u32x8 xv[NBL];
     float xs[NBL];
 #pragma unroll
@@ -203,27 +285,25 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
         }
     }
 
-    // ---- block dots, SiLU(g) * u --------------------------------------------
+    // ---- block dots: OPW gate rows and OPW up rows ----------------------------
+    float part[NV];
 #pragma unroll
-    for (int i = 0; i < OPW; ++i) {
-        const int rg = warp * OPW + i;  // gate row within the slab; up row = rg + 32
-        float g = 0.0f, u = 0.0f;
+    for (int i = 0; i < NV; ++i) {
+        float a = 0.0f;
 #pragma unroll
-        for (int j = 0; j < NBL; ++j) {
-            const int blk = lane + 32 * j;
-            if (blk < nb) {
-                g = block_term(ld_block_halves(s_w + rg * K + blk * QK, c0), xv[j], h2f(s_wd[rg * nb + blk]), xs[j], g);
-                u = block_term(ld_block_halves(s_w + (rg + 32) * K + blk * QK, c0), xv[j],
-                               h2f(s_wd[(rg + 32) * nb + blk]), xs[j], u);
-            }
-        }
-        g = warp_sum(g);
-        u = warp_sum(u);
-        if (lane == 0) {
-            const float hv = silu_mul(g, u);
-            s_h[rg] = hv;
-            p.h[ob + rg] = hv;
-        }
+        for (int j = 0; j < NBL; ++j) a = block_term(wr[i][j], xv[j], wsc[i][j], xs[j], a);
+        part[i] = a;
+    }
+    const float tot_row = warp_sum_many<NV>(part, lane);
+    // lane holds value index (lane & 16 ? NV/2 : 0) + ...: the gate of output i
+    // sits in a lane with bit 4 clear, its up value in the lane with bit 4 set.
+    const float up = __shfl_xor_sync(0xffffffffu, tot_row, 16);
+    constexpr int REP = 32 / NV;  // lanes holding the same value
+    if ((lane & 16) == 0 && (lane & (REP - 1)) == 0) {
+        const int i = (lane & 15) / REP;  // output within the warp
+        const float hv = silu_mul(tot_row, up);
+        s_h[warp * OPW + i] = hv;
+        p.h[ob + warp * OPW + i] = hv;
     }
     __syncthreads();
 
@@ -231,8 +311,8 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
     if (warp == 0) {
         const float v = s_h[lane];
         const float m = warp_max(fabsf(v));
-        const float dd = __fdiv_rn(m, 127.0f);
-        p.hq[ob + lane] = static_cast<int8_t>(q8_code(v, dd));
+        const float dd = div127(m);
+        p.hq[ob + lane] = static_cast<int8_t>(q8_code(v, dd, __frcp_rn(dd)));
         if (lane == 0) p.hd[blockIdx.x] = f2h_rn(dd);
     }
 }
@@ -268,10 +348,17 @@ __global__ void __launch_bounds__(256) gemv_prefetch_kernel(const PrefetchParams
     const int64_t r0 = static_cast<int64_t>(blockIdx.x) * R;
     const int nrow = static_cast<int>(p.n_rows - r0 < R ? p.n_rows - r0 : R);
 
+    __shared__ __align__(8) uint64_t s_bar;
     pdl_trigger();
-    stage_rows(reinterpret_cast<uint8_t *>(s_w), p.w_qs, r0, nrow, K);
-    stage_rows(reinterpret_cast<uint8_t *>(s_wd), p.w_d, r0, nrow, 2 * nb);
-    cp_async_commit();
+    if (threadIdx.x == 0) mbar_init(&s_bar, 1);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint64_t pol = l2_evict_first_policy();
+        const uint32_t vbytes = static_cast<uint32_t>(nrow) * K, sbytes = static_cast<uint32_t>(nrow) * 2 * nb;
+        mbar_expect_tx(&s_bar, vbytes + sbytes);
+        bulk_copy_g2s(s_wd, p.w_d + r0 * nb, sbytes, &s_bar, pol);
+        bulk_copy_g2s(s_w, p.w_qs + r0 * K, vbytes, &s_bar, pol);
+    }
 
     pdl_wait();
 
@@ -289,18 +376,30 @@ __global__ void __launch_bounds__(256) gemv_prefetch_kernel(const PrefetchParams
             xs[j] = 0.0f;
         }
     }
-    cp_async_wait<0>();
-    __syncthreads();
+    if (!__syncthreads_and(mbar_wait_bounded(&s_bar, 0, kCopyWaitLimitNs))) {
+        for (int rr = warp; rr < nrow; rr += nw)
+            if (lane == 0) p.y[r0 + rr] = __int_as_float(0x7fc00000);
+        mbar_wait_bounded(&s_bar, 0, kCopyWaitLimitNs);
+        return;
+    }
 
     for (int rr = warp; rr < nrow; rr += nw) {
-        float acc = 0.0f;
+        u32x8 wr[NBL];
+        float wsc[NBL];
 #pragma unroll
         for (int j = 0; j < NBL; ++j) {
             const int blk = lane + 32 * j;
-            if (blk < nb)
-                acc = block_term(ld_block_halves(s_w + rr * K + blk * QK, c0), xv[j], h2f(s_wd[rr * nb + blk]), xs[j],
-                                 acc);
+            if (blk < nb) {
+                wr[j] = ld_block_halves(s_w + rr * K + blk * QK, c0);
+                wsc[j] = h2f(s_wd[rr * nb + blk]);
+            } else {
+                zero(wr[j]);
+                wsc[j] = 0.0f;
+            }
         }
+        float acc = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NBL; ++j) acc = block_term(wr[j], xv[j], wsc[j], xs[j], acc);
         acc = warp_sum(acc);
         if (lane == 0) {
             const int64_t row = r0 + rr;
@@ -352,6 +451,7 @@ cudaError_t launch_ffn_up(const float *x, const float *gamma, int64_t k, float e
     p.k = static_cast<int>(k);
     p.nb = static_cast<int>(k / QK);
     p.half = half;
+    p.inv_k = 1.0f / static_cast<float>(k);
     p.eps = eps;
     const dim3 grid(static_cast<unsigned>(half / 32));
     const size_t smem = ffn_up_smem_bytes(p.k);

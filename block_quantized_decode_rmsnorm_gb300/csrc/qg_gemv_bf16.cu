@@ -34,6 +34,7 @@ struct Bf16Params {
     int64_t half;
     int k;
     int n_groups;  // k / 8
+    float inv_k;   // fl(1 / k)
     float eps;
     int epi;
 };
@@ -130,7 +131,7 @@ __global__ void __launch_bounds__(BF16_THREADS) gemv_bf16_kernel(const Bf16Param
                 pair_add_square(acc, bf16_hi(u[i]));
             }
         }
-        r = block_rms_inv(acc, p.k, p.eps, scratch);
+        r = block_rms_inv(acc, p.k, p.inv_k, p.eps, scratch);
     }
     for (int g = threadIdx.x; g < p.n_groups; g += blockDim.x) {
         const uint4 xv = ld_16B(p.x + g * 8);
@@ -256,6 +257,7 @@ cudaError_t launch_gemv_bf16(const uint16_t *w, int64_t n_rows, int64_t k, const
     p.n_out = (epi == QG_EPI_SILU_MUL_HALVES) ? n_rows / 2 : n_rows;
     p.k = static_cast<int>(k);
     p.n_groups = static_cast<int>(k / 8);
+    p.inv_k = 1.0f / static_cast<float>(k);
     p.eps = eps;
     p.epi = epi;
     const bool silu = epi == QG_EPI_SILU_MUL_HALVES;

@@ -8,8 +8,9 @@
 //    e = fma(x, x, -p); Dekker's product) and adds both parts into a
 //    compensated pair (hi, lo) with Knuth's two-sum; pairs are merged across the
 //    warp and the block the same way;
-//  * mean = s / k as a pair (the division's remainder is exact through an FMA),
-//    plus eps with a two-sum;
+//  * mean = s / k as a pair: m_hi = fl(s_hi * fl(1/k)) (any value within a few
+//    ulp of s_hi / k will do), the remainder s_hi - m_hi k is exact through an
+//    FMA, m_lo = (remainder + s_lo) / k to f32 accuracy; plus eps with a two-sum;
 //  * y0 = rsqrtf(a), then one Newton-Taylor step r = y0 (1 + e/2 + 3e^2/8) with
 //    the residual e = 1 - a y0^2 evaluated from exact products, and one final
 //    f32 rounding.
@@ -73,13 +74,13 @@ __device__ __forceinline__ f32pair warp_pair_sum(f32pair v)
     return v;
 }
 
-// r from the pair sum of squares (one thread).
-__device__ __forceinline__ float rms_inv_from_pair(f32pair s, int k, float eps)
+// r from the pair sum of squares; inv_k = fl(1 / k).
+__device__ __forceinline__ float rms_inv_from_pair(f32pair s, int k, float inv_k, float eps)
 {
     const float kf = static_cast<float>(k);  // exact: k < 2^24
-    const float m_hi = __fdiv_rn(s.hi, kf);
+    const float m_hi = __fmul_rn(s.hi, inv_k);
     const float rem = __fmaf_rn(-m_hi, kf, s.hi);  // s.hi - m_hi * k, exact
-    const float m_lo = __fdiv_rn(__fadd_rn(rem, s.lo), kf);
+    const float m_lo = __fmul_rn(__fadd_rn(rem, s.lo), inv_k);
     float a_hi, a_e;
     two_sum(m_hi, eps, a_hi, a_e);
     float a_lo = __fadd_rn(a_e, m_lo);
@@ -103,7 +104,7 @@ __device__ __forceinline__ float rms_inv_from_pair(f32pair s, int k, float eps)
 
 // Block-wide: every thread passes its pair; returns r to every thread.
 // `scratch` holds 2 * (blockDim.x / 32) + 1 floats; all threads must call.
-__device__ __forceinline__ float block_rms_inv(f32pair v, int k, float eps, float *scratch)
+__device__ __forceinline__ float block_rms_inv(f32pair v, int k, float inv_k, float eps, float *scratch)
 {
     v = warp_pair_sum(v);
     const int warp = threadIdx.x >> 5;
@@ -116,7 +117,7 @@ __device__ __forceinline__ float block_rms_inv(f32pair v, int k, float eps, floa
     if (threadIdx.x == 0) {
         f32pair t = {scratch[0], scratch[1]};
         for (int w = 1; w < nw; ++w) t = pair_merge(t, f32pair{scratch[2 * w], scratch[2 * w + 1]});
-        scratch[2 * nw] = rms_inv_from_pair(t, k, eps);
+        scratch[2 * nw] = rms_inv_from_pair(t, k, inv_k, eps);
     }
     __syncthreads();
     return scratch[2 * nw];

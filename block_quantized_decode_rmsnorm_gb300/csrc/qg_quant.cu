@@ -28,12 +28,8 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restri
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
     if (!live) return;
-    const float dd = __fdiv_rn(m, 127.0f);
-    const uint32_t c0 = static_cast<uint32_t>(q8_code(v.x, dd)) & 0xffu;
-    const uint32_t c1 = static_cast<uint32_t>(q8_code(v.y, dd)) & 0xffu;
-    const uint32_t c2 = static_cast<uint32_t>(q8_code(v.z, dd)) & 0xffu;
-    const uint32_t c3 = static_cast<uint32_t>(q8_code(v.w, dd)) & 0xffu;
-    reinterpret_cast<uint32_t *>(q + blk * QK)[sub] = c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
+    const float dd = div127(m);
+    reinterpret_cast<uint32_t *>(q + blk * QK)[sub] = q8_pack4(v, dd, __frcp_rn(dd));
     if (sub == 0) d[blk] = f2h_rn(dd);
 }
 
@@ -45,8 +41,8 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restri
 constexpr int NORM_THREADS = 256;
 
 __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_quantize_kernel(
-    const float *__restrict__ x, const float *__restrict__ gamma, int k, float eps, int8_t *__restrict__ q,
-    uint16_t *__restrict__ d, float *__restrict__ inv_rms)
+    const float *__restrict__ x, const float *__restrict__ gamma, int k, float inv_k, float eps,
+    int8_t *__restrict__ q, uint16_t *__restrict__ d, float *__restrict__ inv_rms)
 {
     __shared__ float scratch[2 * (NORM_THREADS / 32) + 1];
     pdl_wait();
@@ -61,7 +57,7 @@ __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_quantize_kernel(
         pair_add_square(acc, v.z);
         pair_add_square(acc, v.w);
     }
-    const float r = block_rms_inv(acc, k, eps, scratch);
+    const float r = block_rms_inv(acc, k, inv_k, eps, scratch);
     if (threadIdx.x == 0 && inv_rms) inv_rms[row] = r;
     // quantize x_hat = (x * r) * gamma, eight lanes per block
     const int nb = k / QK;
@@ -83,13 +79,9 @@ __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_quantize_kernel(
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
         if (live) {
-            const float dd = __fdiv_rn(m, 127.0f);
-            const uint32_t c0 = static_cast<uint32_t>(q8_code(v.x, dd)) & 0xffu;
-            const uint32_t c1 = static_cast<uint32_t>(q8_code(v.y, dd)) & 0xffu;
-            const uint32_t c2 = static_cast<uint32_t>(q8_code(v.z, dd)) & 0xffu;
-            const uint32_t c3 = static_cast<uint32_t>(q8_code(v.w, dd)) & 0xffu;
+            const float dd = div127(m);
             int8_t *qb = q + static_cast<int64_t>(row) * k + b * QK;
-            reinterpret_cast<uint32_t *>(qb)[sub] = c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
+            reinterpret_cast<uint32_t *>(qb)[sub] = q8_pack4(v, dd, __frcp_rn(dd));
             if (sub == 0) d[static_cast<int64_t>(row) * nb + b] = f2h_rn(dd);
         }
     }
@@ -135,7 +127,7 @@ cudaError_t launch_rmsnorm_quantize(const float *x, const float *gamma, int64_t 
 {
     if (rows == 0) return cudaSuccess;
     return launch_pdl(rmsnorm_quantize_kernel, dim3(static_cast<unsigned>(rows)), dim3(NORM_THREADS), 0, s, x,
-                      gamma, static_cast<int>(k), eps, q, d, inv_rms);
+                      gamma, static_cast<int>(k), 1.0f / static_cast<float>(k), eps, q, d, inv_rms);
 }
 
 cudaError_t launch_pack_q8_0(const void *blocks, int64_t n_rows, int64_t k, int8_t *qs, uint16_t *d,
