@@ -268,20 +268,31 @@ def extra_configs(torch, pk) -> dict:
                                              "frac_hbm": algo / t / 1e9 / hbm, "bytes": algo, "copies": copies}
     del ws, g
 
-    # prompt-sized contraction
+    # prompt-sized contraction: tensor-core path (activation tiles, tcgen05) at
+    # the library's tile width and at each fixed one, and the int8 mma.sync
+    # path, on the same rotating weight copies
     pc = synth.prefill_case(0)
     wp = api.q8_weight_from_numpy(pc["w_qs"], pc["w_d"])
     copies = l2_copies(torch, wp.nbytes)
     wps = replicate_q8(torch, api, wp, copies)
-    xq, xd = api.quantize_act_q8_0(torch.from_numpy(pc["x"]).cuda())
+    xdev = torch.from_numpy(pc["x"]).cuda()
+    xq, xd = api.quantize_act_q8_0(xdev)
+    xt = api.quantize_act_q8_0_tiles(xdev)
     yp = torch.empty((512, 7168), dtype=torch.float32, device="cuda")
-    g = capture(torch, lambda: [api.qgemm_q8_0_prefill(w, xq, xd, y=yp) for w in wps])
-    t = time_graph(torch, g, 5) / copies
     ops = 2 * 512 * 7168 * 1024
-    tops = ops / t / 1e12
-    out["prefill_512x7168x1024"] = {"us": t * 1e6, "TOPS": tops, "frac_bf16_dense_peak": tops / pk["bf16_tflops"],
-                                    "int_ops": ops, "path": "mma.sync m16n8k32 s8", "copies": copies}
-    del wps, g
+    variants = [("prefill_512x7168x1024_tcgen05", lambda w: api.qgemm_q8_0_prefill_tc(w, xt, y=yp))]
+    for bn in (64, 96, 128):
+        variants.append((f"prefill_512x7168x1024_tcgen05_bn{bn}",
+                         lambda w, bn=bn: api.qgemm_q8_0_prefill_tc(w, xt, y=yp, tile_n=bn)))
+    variants.append(("prefill_512x7168x1024_mma_sync", lambda w: api.qgemm_q8_0_prefill(w, xq, xd, y=yp)))
+    for name, fn in variants:
+        g = capture(torch, lambda: [fn(w) for w in wps])
+        t = time_graph(torch, g, 5) / copies
+        tops = ops / t / 1e12
+        out[name] = {"us": t * 1e6, "TOPS": tops, "frac_f16_dense_peak": tops / pk["bf16_tflops"], "int_ops": ops,
+                     "copies": copies}
+        del g
+    del wps
     torch.cuda.empty_cache()
     _ = np
     return out

@@ -28,10 +28,13 @@ SIGNATURES = {
     "qg_abi_version": (I32, []),
     "qg_q8_0_pack": (ST, [P, I64, I64, P, P, P]),
     "quantize_act_q8_0": (ST, [P, I64, I64, P, P, P]),
+    "qg_act_tiles_bytes": (I64, [I64, I64]),
+    "quantize_act_q8_0_tiles": (ST, [P, I64, I64, P, P]),
     "rmsnorm_quantize": (ST, [P, P, I64, I64, F32, P, P, P, P]),
     "qgemv_q8_0": (ST, [P, P, I64, I64, P, P, I64, I32, P, P, P]),
     "qgemv_bf16": (ST, [P, I64, I64, P, P, F32, I32, P, P, P]),
     "qgemm_q8_0_prefill": (ST, [P, P, I64, I64, P, P, I64, P, P]),
+    "qgemm_q8_0_prefill_tc": (ST, [P, P, I64, I64, P, I64, P, I32, P]),
     "qg_ffn_up_q8_0": (ST, [P, P, I64, F32, P, P, I64, P, P, P, P, P, P, P]),
     "qg_decode_ffn_q8_0": (ST, [P, P, I64, I64, F32, P, P, P, P, P, P, P, P]),
     "qg_debug_block_dots_q8_0": (ST, [P, I64, I64, P, I64, P, P]),

@@ -109,6 +109,39 @@ def quantize_act_q8_0(x: torch.Tensor, q: torch.Tensor | None = None, d: torch.T
     return q, d
 
 
+class ActTiles:
+    """Activation operand of qgemm_q8_0_prefill_tc: `rows` rows of width `k` as
+    tensor-core tiles (a uint8 device buffer of qg_act_tiles_bytes(rows, k))."""
+
+    def __init__(self, buf: torch.Tensor, rows: int, k: int):
+        self.buf, self.rows, self.k = buf, rows, k
+
+    @staticmethod
+    def nbytes(rows: int, k: int) -> int:
+        n = _lib.load().qg_act_tiles_bytes(rows, k)
+        if n < 0:
+            raise ValueError(f"activation tiles: unsupported shape rows={rows} k={k}")
+        return n
+
+    @classmethod
+    def empty(cls, rows: int, k: int, device) -> "ActTiles":
+        return cls(torch.empty((cls.nbytes(rows, k),), dtype=torch.uint8, device=device), rows, k)
+
+
+def quantize_act_q8_0_tiles(x: torch.Tensor, out: ActTiles | None = None, stream=None) -> ActTiles:
+    """f32 [rows, k] -> Q8_0 codes and scales as tensor-core activation tiles."""
+    _need(x, "x", torch.float32)
+    x2 = _as_2d(x)
+    rows, k = x2.shape
+    if out is None:
+        out = ActTiles.empty(rows, k, x.device)
+    if (out.rows, out.k) != (rows, k) or out.buf.numel() != ActTiles.nbytes(rows, k):
+        raise ValueError("quantize_act_q8_0_tiles: output tiles of another shape")
+    _need(out.buf, "out.buf", torch.uint8)
+    _lib.call("quantize_act_q8_0_tiles", x2.data_ptr(), rows, k, out.buf.data_ptr(), _stream_handle(stream))
+    return out
+
+
 def rmsnorm_quantize(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6, q=None, d=None, inv_rms=None,
                      stream=None):
     """RMSNorm(x) * gamma quantized to Q8_0; returns (q, d, inv_rms)."""
@@ -187,6 +220,24 @@ def qgemm_q8_0_prefill(w: Q8Weight, xq: torch.Tensor, xd: torch.Tensor, y: torch
     _need(y, "y", torch.float32, (m, n_rows))
     _lib.call("qgemm_q8_0_prefill", w.qs.data_ptr(), w.d.data_ptr(), n_rows, k, xq.data_ptr(), xd.data_ptr(), m,
               y.data_ptr(), _stream_handle(stream))
+    return y
+
+
+def qgemm_q8_0_prefill_tc(w: Q8Weight, xt: ActTiles, y: torch.Tensor | None = None, tile_n: int = 0,
+                          stream=None) -> torch.Tensor:
+    """Tensor-core prompt contraction; Y f32 [m, n_rows] from activation tiles of m rows."""
+    _need(w.qs, "w.qs", torch.int8)
+    n_rows, k = w.qs.shape
+    _need(w.d, "w.d", torch.float16, (n_rows, k // 32))
+    if xt.k != k:
+        raise ValueError(f"qgemm_q8_0_prefill_tc: activation width {xt.k} != weight width {k}")
+    _need(xt.buf, "xt.buf", torch.uint8)
+    m = xt.rows
+    if y is None:
+        y = torch.empty((m, n_rows), dtype=torch.float32, device=w.qs.device)
+    _need(y, "y", torch.float32, (m, n_rows))
+    _lib.call("qgemm_q8_0_prefill_tc", w.qs.data_ptr(), w.d.data_ptr(), n_rows, k, xt.buf.data_ptr(), m,
+              y.data_ptr(), tile_n, _stream_handle(stream))
     return y
 
 

@@ -21,6 +21,10 @@ bool ffn_up_supported(int64_t k, int64_t half);
 cudaError_t launch_ffn_up(const float *, const float *, int64_t, float, const int8_t *, const uint16_t *, int64_t,
                           float *, int8_t *, uint16_t *, int8_t *, uint16_t *, float *, cudaStream_t);
 bool prefetch_supported(int64_t n_rows, int64_t k);
+cudaError_t launch_quantize_act_tiles(const float *, int64_t, int64_t, void *, cudaStream_t);
+bool prefill_tc_supported(int64_t k);
+cudaError_t launch_prefill_tc(const int8_t *, const uint16_t *, int64_t, int64_t, const void *, int64_t, float *, int,
+                              cudaStream_t);
 cudaError_t launch_gemv_prefetch(const int8_t *, const uint16_t *, int64_t, int64_t, const int8_t *, const uint16_t *,
                                  int, const float *, float *, cudaStream_t);
 
@@ -98,6 +102,30 @@ qg_status quantize_act_q8_0(const float *x, int64_t rows, int64_t k, int8_t *q, 
     if (!x || !q || !d) return QG_ERR_NULL;
     if (!aligned(x, 16) || !aligned(q, 16) || !aligned(d, 2)) return QG_ERR_ALIGN;
     return from_cuda(qg::launch_quantize_act(x, rows, k, q, d, stream));
+}
+
+// Activation tiles: rows up to 2^24, and (tiles x blocks x 4) warps' worth of
+// 8-lane groups must fit one launch grid.
+static bool act_tiles_shape_ok(int64_t rows, int64_t k)
+{
+    if (rows < 0 || rows > (int64_t(1) << 24) || k <= 0 || k > kMaxK) return false;
+    return qg::act_tiles(rows) * (k / qg::QK) * 4 < (int64_t(1) << 31);
+}
+
+int64_t qg_act_tiles_bytes(int64_t rows, int64_t k)
+{
+    if (k % qg::QK != 0 || !act_tiles_shape_ok(rows, k)) return -1;
+    return qg::act_tiles(rows) * (k / qg::QK) * qg::ACT_TILE_RECORD;
+}
+
+qg_status quantize_act_q8_0_tiles(const float *x, int64_t rows, int64_t k, void *xt, qg_stream_t stream)
+{
+    if (qg_status st = check_q8_k(k); st != QG_OK) return st;
+    if (!act_tiles_shape_ok(rows, k)) return QG_ERR_SHAPE;
+    if (rows == 0) return QG_OK;
+    if (!x || !xt) return QG_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(xt, 16)) return QG_ERR_ALIGN;
+    return from_cuda(qg::launch_quantize_act_tiles(x, rows, k, xt, stream));
 }
 
 qg_status rmsnorm_quantize(const float *x, const float *gamma, int64_t rows, int64_t k, float eps, int8_t *q,
@@ -205,6 +233,20 @@ qg_status qg_decode_ffn_q8_0(float *x, const float *gamma, int64_t hidden, int64
         return from_cuda(qg::launch_gemv_prefetch(wdn_qs, wdn_d, hidden, ffn, hq, hd, QG_EPI_RESIDUAL_ADD, x, x,
                                                   stream));
     return from_cuda(qg::launch_gemv_q8_0(wdn_qs, wdn_d, hidden, ffn, hq, hd, 1, QG_EPI_RESIDUAL_ADD, x, x, stream));
+}
+
+qg_status qgemm_q8_0_prefill_tc(const int8_t *w_qs, const uint16_t *w_d, int64_t n_rows, int64_t k, const void *xt,
+                                int64_t m, float *y, int32_t tile_n, qg_stream_t stream)
+{
+    if (n_rows < 0 || n_rows > kMaxRows || n_rows > UINT32_MAX / 2) return QG_ERR_SHAPE;
+    if (qg_status st = check_q8_k(k); st != QG_OK) return st;
+    if (!act_tiles_shape_ok(m, k)) return QG_ERR_SHAPE;
+    if (!qg::prefill_tc_supported(k)) return QG_ERR_UNSUPPORTED;
+    if (tile_n != 0 && tile_n != 64 && tile_n != 96 && tile_n != 128) return QG_ERR_UNSUPPORTED;
+    if (n_rows == 0 || m == 0) return QG_OK;
+    if (!w_qs || !w_d || !xt || !y) return QG_ERR_NULL;
+    if (!aligned(w_qs, 32) || !aligned(w_d, 16) || !aligned(xt, 16) || !aligned(y, 16)) return QG_ERR_ALIGN;
+    return from_cuda(qg::launch_prefill_tc(w_qs, w_d, n_rows, k, xt, m, y, tile_n, stream));
 }
 
 qg_status qg_debug_block_dots_q8_0(const int8_t *w_qs, int64_t n_rows, int64_t k, const int8_t *xq, int64_t batch,

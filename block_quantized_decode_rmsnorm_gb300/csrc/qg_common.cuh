@@ -16,6 +16,13 @@ namespace qg {
 
 constexpr int QK = 32;  // values per Q8_0 block
 
+// Operand tiles of the tensor-core prompt contraction: activation rows in tiles
+// of 128; per tile and block one record of 4 x 2048 bytes of binary16 codes and
+// 128 binary16 scales.
+constexpr int ACT_TILE_ROWS = 128;
+constexpr int ACT_TILE_RECORD = 8192 + 256;
+__host__ __device__ inline int64_t act_tiles(int64_t rows) { return (rows + ACT_TILE_ROWS - 1) / ACT_TILE_ROWS; }
+
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch.  A kernel launched with the programmatic
 // stream serialization attribute may begin before its predecessor ends; it

@@ -9,12 +9,11 @@
 namespace qg {
 
 // x[rows][k] -> q[rows][k], d[rows][k/32].  Eight lanes per 32-value block,
-// four values per lane (one 16-byte load of x and one 4-byte store of codes per
+// four values per lane (one 16-byte load of x and one store of codes per
 // lane); a warp covers four blocks.  Lanes past the end take part in the
 // shuffles with zeros and skip the stores.
 __global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restrict__ x, int64_t n_blocks,
-                                                                 int8_t *__restrict__ q,
-                                                                 uint16_t *__restrict__ d)
+                                                           int8_t *__restrict__ q, uint16_t *__restrict__ d)
 {
     pdl_wait();
     pdl_trigger();
@@ -29,8 +28,47 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restri
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
     if (!live) return;
     const float dd = div127(m);
-    reinterpret_cast<uint32_t *>(q + blk * QK)[sub] = q8_pack4(v, dd, __frcp_rn(dd));
+    const float rd = __frcp_rn(dd);
+    reinterpret_cast<uint32_t *>(q + blk * QK)[sub] = q8_pack4(v, dd, rd);
     if (sub == 0) d[blk] = f2h_rn(dd);
+}
+
+// The same quantization written as the operand tiles of the tensor-core prompt
+// contraction: for each tile of 128 rows and each block j one record of
+// ACT_TILE_RECORD bytes, the codes as binary16 values (exact: |q| <= 127) in
+// four groups of eight, code 8g+e of tile row r at byte 2048 g + 16 r + 2 e,
+// then the 128 binary16 scales.  Rows past the end of the last tile are zero.
+// Eight lanes per (row, block) with the tile row fastest, so a warp's stores
+// fill 64 contiguous bytes of each group.
+__global__ void __launch_bounds__(256) quantize_act_tiles_kernel(const float *__restrict__ x, int64_t rows, int nb,
+                                                                 int64_t n_groups, uint8_t *__restrict__ xt)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int64_t gidx = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 3;
+    if (gidx >= n_groups) return;  // n_groups is a multiple of 128: whole warps leave together
+    const int sub = threadIdx.x & 7;
+    const int r = static_cast<int>(gidx & (ACT_TILE_ROWS - 1));
+    const int64_t rec = gidx >> 7;  // tile * nb + block
+    const int64_t tile = rec / nb;
+    const int j = static_cast<int>(rec - tile * nb);
+    const int64_t row = tile * ACT_TILE_ROWS + r;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row < rows) v = *reinterpret_cast<const float4 *>(x + (row * nb + j) * QK + sub * 4);
+    float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    const float dd = div127(m);
+    const float rd = __frcp_rn(dd);
+    const uint32_t c0 = __half_as_ushort(__int2half_rn(q8_code(v.x, dd, rd)));
+    const uint32_t c1 = __half_as_ushort(__int2half_rn(q8_code(v.y, dd, rd)));
+    const uint32_t c2 = __half_as_ushort(__int2half_rn(q8_code(v.z, dd, rd)));
+    const uint32_t c3 = __half_as_ushort(__int2half_rn(q8_code(v.w, dd, rd)));
+    uint8_t *base = xt + rec * ACT_TILE_RECORD;
+    *reinterpret_cast<uint2 *>(base + (sub >> 1) * 2048 + r * 16 + (sub & 1) * 8) =
+        make_uint2(c0 | (c1 << 16), c2 | (c3 << 16));
+    if (sub == 0) *reinterpret_cast<uint16_t *>(base + 8192 + r * 2) = f2h_rn(dd);
 }
 
 // One CTA per row.  r = 1/sqrt(mean(x^2) + eps) evaluated as in f64 and rounded
@@ -120,6 +158,16 @@ cudaError_t launch_quantize_act(const float *x, int64_t rows, int64_t k, int8_t 
     const int64_t threads = n_blocks * 8;
     const unsigned grid = static_cast<unsigned>((threads + 255) / 256);
     return launch_pdl(quantize_act_kernel, dim3(grid), dim3(256), 0, s, x, n_blocks, q, d);
+}
+
+cudaError_t launch_quantize_act_tiles(const float *x, int64_t rows, int64_t k, void *xt, cudaStream_t s)
+{
+    const int nb = static_cast<int>(k / QK);
+    const int64_t n_groups = act_tiles(rows) * nb * ACT_TILE_ROWS;
+    if (n_groups == 0) return cudaSuccess;
+    const unsigned grid = static_cast<unsigned>((n_groups * 8 + 255) / 256);
+    return launch_pdl(quantize_act_tiles_kernel, dim3(grid), dim3(256), 0, s, x, rows, nb, n_groups,
+                      static_cast<uint8_t *>(xt));
 }
 
 cudaError_t launch_rmsnorm_quantize(const float *x, const float *gamma, int64_t rows, int64_t k, float eps,

@@ -106,6 +106,28 @@ QG_API qg_status quantize_act_q8_0(const float *x, int64_t rows, int64_t k,
                             int8_t *q, uint16_t *d, qg_stream_t stream);
 
 /*
+ * quantize_act_q8_0_tiles - the Q8_0 quantization of quantize_act_q8_0 (same
+ * codes, same scales), written as the activation operand of the tensor-core
+ * prompt contraction qgemm_q8_0_prefill_tc ([Phobos] Fast Decode: prompt
+ * processing runs on the tensor cores).  The pages store codes as int8; this
+ * form holds each code as a binary16 value (exact: an integer in [-127, 127])
+ * already in the order the tensor core reads, so the contraction copies it
+ * without conversion.
+ *   Layout: rows in tiles of 128 (rows past `rows` in the last tile are zero);
+ *   for tile t and block j one record of 8448 bytes at byte offset
+ *   (t * (k/32) + j) * 8448:
+ *     bytes [0, 8192):    code 8g+e (g < 4, e < 8) of tile row r as binary16 at
+ *                         byte 2048 g + 16 r + 2 e;
+ *     bytes [8192, 8448): the 128 binary16 scales of the tile rows.
+ *   x:  device f32[rows][k] (read), 16-byte aligned; rows <= 2^24
+ *   xt: device, qg_act_tiles_bytes(rows, k) bytes (written), 16-byte aligned;
+ *       caller-owned.
+ */
+QG_API int64_t qg_act_tiles_bytes(int64_t rows, int64_t k);  /* -1: shape unsupported */
+QG_API qg_status quantize_act_q8_0_tiles(const float *x, int64_t rows, int64_t k, void *xt,
+                                         qg_stream_t stream);
+
+/*
  * rmsnorm_quantize - RMSNorm followed by Q8_0 quantization of each row.
  * [Herbert] Emitting for a GPU (normalization fused with the projection that
  * follows it); [Phobos] Q4_K_M (the fast norm kernel).
@@ -203,6 +225,27 @@ QG_API qg_status qg_decode_ffn_q8_0(float *x, const float *gamma, int64_t hidden
                                     float eps, const int8_t *wgu_qs, const uint16_t *wgu_d,
                                     const int8_t *wdn_qs, const uint16_t *wdn_d, float *h,
                                     int8_t *hq, uint16_t *hd, qg_stream_t stream);
+
+/*
+ * qgemm_q8_0_prefill_tc - the prompt contraction of qgemm_q8_0_prefill on the
+ * tcgen05 tensor cores ([Phobos] Fast Decode: prompt processing belongs on the
+ * tensor cores; GPU Performance Heisenbugs: exact integer values on the tensor
+ * cores).  Exact int8 codes run as f16 operands, the exact block sums land in
+ * the f32 accumulator, and the block scales are applied per block:
+ *   Y[m][n] = sum_j f32(d_x[m][j]) * f32(d_w[n][j]) * S_j[m][n].
+ *   w_qs: device int8[n_rows][k] (read), 32-byte aligned
+ *   w_d:  device binary16 bits [n_rows][k/32] (read), 16-byte aligned
+ *   xt:   activation tiles of m rows from quantize_act_q8_0_tiles (read)
+ *   y:    device f32[m][n_rows] (written), 16-byte aligned
+ *   k a multiple of 256 (QG_ERR_UNSUPPORTED otherwise); m <= 2^24.
+ *   tile_n: output tile width 64, 96 or 128, or 0 to let the library choose.
+ *   Runs one CTA per SM over all output tiles.  If an operand copy stalls
+ *   beyond one second the kernel stops waiting and writes NaN for the tiles
+ *   it has left, rather than hanging.
+ */
+QG_API qg_status qgemm_q8_0_prefill_tc(const int8_t *w_qs, const uint16_t *w_d, int64_t n_rows,
+                                       int64_t k, const void *xt, int64_t m, float *y,
+                                       int32_t tile_n, qg_stream_t stream);
 
 /*
  * qg_debug_block_dots_q8_0 - the exact per-block int32 sums, for parity checks.

@@ -115,3 +115,30 @@ def test_fused_ffn_argument_errors(lib):
     assert d(FAKE, FAKE, 1024, 3584, eps, FAKE, FAKE, FAKE, FAKE + 2, FAKE, FAKE, FAKE, None) == 2
     assert d(FAKE, FAKE, 1024, 3584, eps, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 16, FAKE, None) == 2
     assert d(FAKE, FAKE, 1024, 0, eps, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == 3
+
+
+def test_prefill_tc_argument_errors(lib):
+    tc = lib.qgemm_q8_0_prefill_tc
+    # K must be a multiple of 256 for the tensor-core path
+    assert tc(FAKE, FAKE, 8, 96, FAKE, 1, FAKE, 0, None) == 4
+    # weight scales 16-byte aligned (they are fetched with the tensor-memory accelerator)
+    assert tc(FAKE, FAKE + 2, 8, 256, FAKE, 1, FAKE, 0, None) == 2
+    # tile widths 0 (library's choice), 64, 96, 128 only
+    assert tc(FAKE, FAKE, 8, 256, FAKE, 1, FAKE, 80, None) == 4
+    assert tc(FAKE, FAKE, 8, 256, FAKE, 0, FAKE, 0, None) == 0
+    assert tc(FAKE, FAKE, 8, 256, FAKE, (1 << 24) + 1, FAKE, 0, None) == 3
+    assert tc(None, FAKE, 8, 256, FAKE, 1, FAKE, 0, None) == 1
+
+
+def test_act_tiles_size_and_errors(lib):
+    # one record of 8192 code bytes + 256 scale bytes per (128-row tile, block)
+    assert lib.qg_act_tiles_bytes(130, 256) == 2 * 8 * 8448
+    assert lib.qg_act_tiles_bytes(128, 32) == 8448
+    assert lib.qg_act_tiles_bytes(0, 64) == 0
+    assert lib.qg_act_tiles_bytes(1, 33) == -1
+    assert lib.qg_act_tiles_bytes((1 << 24) + 1, 32) == -1
+    qt = lib.quantize_act_q8_0_tiles
+    assert qt(FAKE, 1, 48, FAKE, None) == 3
+    assert qt(FAKE, 1, 64, FAKE + 8, None) == 2
+    assert qt(None, 1, 64, FAKE, None) == 1
+    assert qt(None, 0, 64, None, None) == 0

@@ -113,3 +113,78 @@ def test_prefill_row_equals_gemv(torch, orc):
     xq, xd = orc.quantize_q8_0(x)
     y64, a64 = orc.gemv_q8_0(qs, d, xq, xd)
     assert_close(yp, yg, a64, 2 * TOL_Q8, "prefill vs gemv")
+
+
+# ---------------------------------------------------------------------------
+# tensor-core path: activation tiles, tcgen05
+# ---------------------------------------------------------------------------
+
+def untile(buf: np.ndarray, rows: int, k: int):
+    """Activation tiles -> (codes f16 [tiles*128, k], scale bits u16 [tiles*128, k/32])."""
+    nb, tiles = k // 32, -(-rows // 128)
+    rec = buf.reshape(tiles, nb, 8448)
+    codes = np.ascontiguousarray(rec[:, :, :8192]).view(np.float16).reshape(tiles, nb, 4, 128, 8)
+    codes = codes.transpose(0, 3, 1, 2, 4).reshape(tiles * 128, k)
+    scales = np.ascontiguousarray(rec[:, :, 8192:]).view(np.uint16).reshape(tiles, nb, 128)
+    return codes, scales.transpose(0, 2, 1).reshape(tiles * 128, nb)
+
+
+@pytest.mark.parametrize("rows,k", [(37, 1024), (128, 256), (129, 512), (1, 32)])
+def test_quantize_act_tiles_bit_exact(torch, orc, rows, k):
+    from block_quantized_decode_rmsnorm_gb300 import api
+
+    x = synth.f32_normal(21 + rows, 0, (rows, k))
+    x[min(3, rows - 1), :32] = 0.0
+    xt = api.quantize_act_q8_0_tiles(to_dev(x, torch))
+    torch.cuda.synchronize()
+    codes, scales = untile(xt.buf.cpu().numpy(), rows, k)
+    qo, do = orc.quantize_q8_0(x)
+    assert np.array_equal(codes[:rows].astype(np.float32), qo.astype(np.float32))
+    assert np.array_equal(scales[:rows], do)
+    assert not codes[rows:].any() and not scales[rows:].any()  # padding rows are zero
+
+
+@pytest.mark.parametrize("m,n,k,tile_n", [
+    (1, 64, 256, 0), (5, 70, 256, 64), (5, 70, 256, 96), (5, 70, 256, 128),
+    (128, 64, 1024, 0), (130, 200, 1024, 96), (256, 128, 3584, 0), (33, 129, 4096, 128),
+    (3, 40, 8192, 64),                        # K beyond one scale table
+    (300, 1000, 512, 64),                     # more tiles than SMs at BN=64: several tiles per CTA
+    (512, 7168, 1024, 0), (512, 7168, 1024, 64), (512, 7168, 1024, 128),
+])
+def test_prefill_tc(torch, orc, m, n, k, tile_n):
+    from block_quantized_decode_rmsnorm_gb300 import api
+
+    qs, d = synth.q8_0_weight_planes(m + 3 * n, 10, n, k)
+    x = synth.f32_normal(m + k + 1, 0, (m, k))
+    xt = api.quantize_act_q8_0_tiles(to_dev(x, torch))
+    gy = Guarded(torch, (m, n), torch.float32)
+    api.qgemm_q8_0_prefill_tc(weight(qs, d), xt, y=gy.view, tile_n=tile_n)
+    torch.cuda.synchronize()
+    gy.check()
+    y = gy.view.cpu().numpy()
+    xq, xdo = orc.quantize_q8_0(x)
+    rows = np.arange(m) if m <= 300 else np.unique(np.concatenate([np.arange(0, m, 37), [m - 1, 127, 128]]))
+    y64, a64 = orc.gemv_q8_0(qs, d, xq[rows], xdo[rows])
+    assert_close(y[rows], y64, a64, TOL_Q8, f"prefill tc {m}x{n}x{k} tile {tile_n}")
+    assert not np.isnan(y).any()
+
+
+def test_prefill_tc_matches_mma_sync_path(torch, orc):
+    """Both prompt-contraction kernels on the same operands agree within the
+    combined tolerance, and the tensor-core one is deterministic across calls."""
+    from block_quantized_decode_rmsnorm_gb300 import api
+
+    m, n, k = 200, 300, 2048
+    qs, d = synth.q8_0_weight_planes(77, 10, n, k)
+    x = synth.f32_normal(78, 0, (m, k))
+    xd_ = to_dev(x, torch)
+    w = weight(qs, d)
+    xt = api.quantize_act_q8_0_tiles(xd_)
+    y1 = api.qgemm_q8_0_prefill_tc(w, xt).cpu().numpy()
+    y2 = api.qgemm_q8_0_prefill_tc(w, xt).cpu().numpy()
+    assert np.array_equal(y1, y2)
+    xq_t, xs_t = api.quantize_act_q8_0(xd_)
+    ym = api.qgemm_q8_0_prefill(w, xq_t, xs_t).cpu().numpy()
+    xq, xdo = orc.quantize_q8_0(x)
+    _, a64 = orc.gemv_q8_0(qs, d, xq, xdo)
+    assert_close(y1, ym, a64, 2 * TOL_Q8, "tc vs mma.sync")
