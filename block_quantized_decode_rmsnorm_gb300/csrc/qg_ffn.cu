@@ -161,18 +161,31 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
     pdl_trigger();
 
     // ---- stage everything that does not depend on the previous kernel -------
-    // (bulk copies: one instruction per contiguous slab, completion on s_bar)
+    // Bulk copies issued by one thread are serviced one after another, so the
+    // slab is cut into pieces (gamma, the two scale slabs, eight value slabs of
+    // eight rows) that lanes 0-10 of warp 0 issue in one instruction; all
+    // complete on s_bar.
     if (t == 0) mbar_init(&s_bar, 1);
     __syncthreads();
-    if (t == 0) {
-        const uint64_t pol = l2_evict_first_policy();
-        const uint32_t vbytes = 32u * K, sbytes = 64u * nb;
-        mbar_expect_tx(&s_bar, 4u * K + 2 * sbytes + 2 * vbytes);
-        bulk_copy_g2s(s_gamma, p.gamma, 4u * K, &s_bar, l2_evict_last_policy());
-        bulk_copy_g2s(s_wd, p.w_d + ob * nb, sbytes, &s_bar, pol);
-        bulk_copy_g2s(s_wd + 32 * nb, p.w_d + (p.half + ob) * nb, sbytes, &s_bar, pol);
-        bulk_copy_g2s(s_w, p.w_qs + ob * K, vbytes, &s_bar, pol);
-        bulk_copy_g2s(s_w + 32 * K, p.w_qs + (p.half + ob) * K, vbytes, &s_bar, pol);
+    if (warp == 0) {
+        constexpr int PR = 8;  // rows per value piece
+        const uint32_t sbytes = 64u * nb;
+        if (lane == 0) mbar_expect_tx(&s_bar, 4u * K + 2 * sbytes + 64u * K);
+        __syncwarp();
+        if (lane < 3 + 64 / PR) {
+            const int v = lane - 3;                      // value piece: rows PR v .. of the stacked 64
+            const int64_t vrow = (v < 32 / PR ? ob : p.half + ob - 32) + static_cast<int64_t>(PR) * v;
+            const int64_t srow = lane == 1 ? ob : p.half + ob;
+            void *dst = lane == 0 ? static_cast<void *>(s_gamma)
+                      : lane < 3  ? static_cast<void *>(s_wd + (lane - 1) * 32 * nb)
+                                  : static_cast<void *>(s_w + PR * v * K);
+            const void *src = lane == 0 ? static_cast<const void *>(p.gamma)
+                            : lane < 3  ? static_cast<const void *>(p.w_d + srow * nb)
+                                        : static_cast<const void *>(p.w_qs + vrow * K);
+            const uint32_t bytes = lane == 0 ? 4u * K : lane < 3 ? sbytes : static_cast<uint32_t>(PR) * K;
+            const uint64_t pol = lane == 0 ? l2_evict_last_policy() : l2_evict_first_policy();
+            bulk_copy_g2s(dst, src, bytes, &s_bar, pol);
+        }
     }
 
     pdl_wait();
@@ -352,16 +365,28 @@ __global__ void __launch_bounds__(256) gemv_prefetch_kernel(const PrefetchParams
     pdl_trigger();
     if (threadIdx.x == 0) mbar_init(&s_bar, 1);
     __syncthreads();
-    if (threadIdx.x == 0) {
-        const uint64_t pol = l2_evict_first_policy();
+    if (warp == 0) {
+        // scales on lane 0, the value slab in up to four row pieces on lanes 1-4,
+        // issued in one instruction (one lane's bulk copies are serviced in turn)
         const uint32_t vbytes = static_cast<uint32_t>(nrow) * K, sbytes = static_cast<uint32_t>(nrow) * 2 * nb;
-        mbar_expect_tx(&s_bar, vbytes + sbytes);
-        bulk_copy_g2s(s_wd, p.w_d + r0 * nb, sbytes, &s_bar, pol);
-        bulk_copy_g2s(s_w, p.w_qs + r0 * K, vbytes, &s_bar, pol);
+        if (lane == 0) mbar_expect_tx(&s_bar, vbytes + sbytes);
+        __syncwarp();
+        const int pr = (nrow + 3) / 4;  // rows per value piece
+        const int v0 = (lane - 1) * pr;
+        const int vr = lane == 0 ? 0 : (nrow - v0 < pr ? nrow - v0 : pr);
+        if (lane == 0 || (lane <= 4 && vr > 0)) {
+            void *dst = lane == 0 ? static_cast<void *>(s_wd) : static_cast<void *>(s_w + static_cast<size_t>(v0) * K);
+            const void *src = lane == 0 ? static_cast<const void *>(p.w_d + r0 * nb)
+                                        : static_cast<const void *>(p.w_qs + (r0 + v0) * K);
+            const uint32_t bytes = lane == 0 ? sbytes : static_cast<uint32_t>(vr) * K;
+            bulk_copy_g2s(dst, src, bytes, &s_bar, l2_evict_first_policy());
+        }
     }
 
     pdl_wait();
 
+    // The activation and, for the residual epilogue, this lane's residual
+    // value are loaded together, so both L2 round trips overlap.
     const int c0 = lane_half(lane);
     u32x8 xv[NBL];
     float xs[NBL];
@@ -376,6 +401,9 @@ __global__ void __launch_bounds__(256) gemv_prefetch_kernel(const PrefetchParams
             xs[j] = 0.0f;
         }
     }
+    // lane l of warp w holds the residual of row w + l * nw (rows of this CTA)
+    float res = 0.0f;
+    if (p.epi == QG_EPI_RESIDUAL_ADD && warp + lane * nw < nrow) res = p.residual[r0 + warp + lane * nw];
     if (!__syncthreads_and(mbar_wait_bounded(&s_bar, 0, kCopyWaitLimitNs))) {
         for (int rr = warp; rr < nrow; rr += nw)
             if (lane == 0) p.y[r0 + rr] = __int_as_float(0x7fc00000);
@@ -383,7 +411,7 @@ __global__ void __launch_bounds__(256) gemv_prefetch_kernel(const PrefetchParams
         return;
     }
 
-    for (int rr = warp; rr < nrow; rr += nw) {
+    for (int rr = warp, it = 0; rr < nrow; rr += nw, ++it) {
         u32x8 wr[NBL];
         float wsc[NBL];
 #pragma unroll
@@ -401,9 +429,12 @@ __global__ void __launch_bounds__(256) gemv_prefetch_kernel(const PrefetchParams
 #pragma unroll
         for (int j = 0; j < NBL; ++j) acc = block_term(wr[j], xv[j], wsc[j], xs[j], acc);
         acc = warp_sum(acc);
+        const float rv = __shfl_sync(0xffffffffu, res, it & 31);
         if (lane == 0) {
             const int64_t row = r0 + rr;
-            p.y[row] = (p.epi == QG_EPI_RESIDUAL_ADD) ? p.residual[row] + acc : acc;
+            float rres = rv;
+            if (p.epi == QG_EPI_RESIDUAL_ADD && it >= 32) rres = p.residual[row];  // more than 32 rows per warp
+            p.y[row] = (p.epi == QG_EPI_RESIDUAL_ADD) ? rres + acc : acc;
         }
     }
 }
