@@ -137,17 +137,23 @@ class ClockSampler:
 # distributed plumbing (one process per GPU; no collective on the data path)
 # --------------------------------------------------------------------------
 class Dist:
-    def __init__(self, torch):
+    """One process per GPU under torchrun: barrier and max-over-ranks timing.
+    NCCL on GPUs; gloo (tensors on the host) when asked, which is how the
+    multi-rank logic is exercised on a CPU-only machine."""
+
+    def __init__(self, torch, backend: str = "nccl"):
         self.torch = torch
         self.world = int(os.environ.get("WORLD_SIZE", "1"))
         self.rank = int(os.environ.get("RANK", "0"))
         self.local = int(os.environ.get("LOCAL_RANK", "0"))
         self.pg = None
+        self.device = "cuda" if backend == "nccl" else "cpu"
         if self.world > 1:
             import torch.distributed as dist
 
-            torch.cuda.set_device(self.local)
-            dist.init_process_group("nccl")
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend)
             self.pg = dist
 
     def barrier(self):
@@ -157,13 +163,19 @@ class Dist:
     def max(self, v: float) -> float:
         if not self.pg:
             return v
-        t = self.torch.tensor([v], dtype=self.torch.float64, device="cuda")
+        t = self.torch.tensor([v], dtype=self.torch.float64, device=self.device)
         self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
         return float(t.item())
 
     def close(self):
         if self.pg:
             self.pg.destroy_process_group()
+
+
+def job_rate(world: int, steps: int, unit_bytes: int, max_elapsed_s: float) -> float:
+    """Whole-job GB/s: every rank processes `steps` units of `unit_bytes`; the
+    job takes as long as its slowest rank."""
+    return world * steps * unit_bytes / max_elapsed_s / 1e9
 
 
 # --------------------------------------------------------------------------
@@ -387,7 +399,7 @@ def run_ours(args):
     dist.barrier()
     elapsed = dist.max(e0.elapsed_time(e1) / 1e3)
     step_bytes = L * LAYER_BYTES
-    value = dist.world * args.steps * step_bytes / elapsed / 1e9
+    value = job_rate(dist.world, args.steps, step_bytes, elapsed)
 
     # dominant kernel: the fused gate|up launch, back to back over the L layers
     h1, hq1, hd1 = buf.h[0], buf.hq[0], buf.hd[0]
@@ -417,7 +429,7 @@ def run_ours(args):
         out_host.copy_(x, non_blocking=True)
         torch.cuda.current_stream().synchronize()
     e2e_el = dist.max(time.perf_counter() - t0)
-    e2e = {"value": dist.world * args.steps * step_bytes / e2e_el / 1e9, "unit": "GB/s",
+    e2e = {"value": job_rate(dist.world, args.steps, step_bytes, e2e_el), "unit": "GB/s",
            "h2d_bytes_per_step": HIDDEN * 4, "d2h_bytes_per_step": HIDDEN * 4,
            "ms_per_step": e2e_el / args.steps * 1e3}
 
