@@ -45,6 +45,8 @@ W_DN_BYTES = HIDDEN * FFN + HIDDEN * (FFN // 32) * 2
 LAYER_BYTES = W_GU_BYTES + W_DN_BYTES + 3 * HIDDEN * 4
 # fused gate|up launch: weights, x and gamma in (f32), h out (f32) and its Q8_0 codes + scales
 GU_KERNEL_BYTES = W_GU_BYTES + 2 * HIDDEN * 4 + FFN * 4 + FFN + (FFN // 32) * 2
+# one-launch layer: both weights, x in, gamma, x out, the cleared buffer, h and its codes and scales
+LAYER_KERNEL_BYTES = W_GU_BYTES + W_DN_BYTES + 4 * HIDDEN * 4 + FFN * 4 + FFN + (FFN // 32) * 2
 
 
 def workload_name(layers: int) -> str:
@@ -370,12 +372,24 @@ def run_ours(args):
     buf = api.FFNBuffers.allocate(HIDDEN, FFN, "cuda")
     x = torch.from_numpy(x0_np).cuda()
 
-    fused = not args.unfused
-    launches_per_layer = 2 if fused else 4
+    path = args.path
+    launches_per_layer = {"one": 1, "two": 2, "four": 4}[path]
+    launches_per_step = launches_per_layer * L + (1 if path == "one" else 0)  # + the finish
+    stack = api.LayerStack(HIDDEN, FFN, "cuda") if path == "one" else None
+    x_out = x
+    if stack is not None:
+        for layer in layers:  # down weights in the column-block layout, packed once at load time
+            api.prepare_one_launch(layer)
+        stack.load(x)
+        torch.cuda.synchronize()
+        x, x_out = stack.r[0], stack.out  # each replay reads r[0] and writes out
 
     def step():
+        if stack is not None:
+            stack.run(layers, buf, EPS)
+            return
         for layer in layers:
-            if fused:
+            if path == "two":
                 api.qg_decode_ffn_q8_0(x, layer, buf, EPS)
             else:
                 api.decode_ffn_q8_0(x, layer, buf, EPS)
@@ -401,17 +415,24 @@ def run_ours(args):
     step_bytes = L * LAYER_BYTES
     value = job_rate(dist.world, args.steps, step_bytes, elapsed)
 
-    # dominant kernel: the fused gate|up launch, back to back over the L layers
-    h1, hq1, hd1 = buf.h[0], buf.hq[0], buf.hd[0]
-    gu_graph = capture(torch, lambda: [api.qg_ffn_up_q8_0(x, l.gamma, l.gate_up, EPS, h=h1, hq=hq1, hd=hd1)
-                                       for l in layers])
-    t_gu = time_graph(torch, gu_graph, max(5, args.steps // 4)) / L
-    achieved = GU_KERNEL_BYTES / t_gu / 1e9
-    roofline = {"bound": "hbm", "kernel": "ffn_up_kernel<1> (RMSNorm + Q8_0 + gate|up 7168x1024 + SiLU*u + Q8_0)",
-                "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
-                "peak_source": pk["source"], "algorithmic_bytes_per_launch": GU_KERNEL_BYTES,
-                "launch_us": t_gu * 1e6, "traffic": ncu_traffic("ffn_up_kernel")}
-    del gu_graph
+    # dominant kernel, timed alone (L back-to-back launches in a graph, events on the launching stream)
+    if path == "one":
+        # the layer kernel is the step's only kernel but the one-block finish
+        t_k = time_graph(torch, g, max(5, args.steps // 4)) / L
+        kbytes, kname, kkey = LAYER_KERNEL_BYTES, ("ffn_up_kernel<1,true> (one-launch layer: RMSNorm + Q8_0 + "
+                                                   "gate|up + SiLU*u + Q8_0 + split-K down + residual)"), "layer_kernel"
+    else:
+        h1, hq1, hd1 = buf.h[0], buf.hq[0], buf.hd[0]
+        gu_graph = capture(torch, lambda: [api.qg_ffn_up_q8_0(x, l.gamma, l.gate_up, EPS, h=h1, hq=hq1, hd=hd1)
+                                           for l in layers])
+        t_k = time_graph(torch, gu_graph, max(5, args.steps // 4)) / L
+        del gu_graph
+        kbytes, kname, kkey = GU_KERNEL_BYTES, "ffn_up_kernel<1> (RMSNorm + Q8_0 + gate|up 7168x1024 + SiLU*u + Q8_0)", \
+            "ffn_up_kernel"
+    achieved = kbytes / t_k / 1e9
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "peak_source": pk["source"], "algorithmic_bytes_per_launch": kbytes,
+                "launch_us": t_k * 1e6, "traffic": ncu_traffic(kkey)}
 
     # end to end through host buffers: H2D of x, the step, D2H of the result, every step
     x_host = torch.from_numpy(x0_np.copy()).pin_memory()
@@ -419,14 +440,14 @@ def run_ours(args):
     for _ in range(max(3, args.warmup)):
         x.copy_(x_host, non_blocking=True)
         g.replay()
-        out_host.copy_(x, non_blocking=True)
+        out_host.copy_(x_out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
     dist.barrier()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         x.copy_(x_host, non_blocking=True)
         g.replay()
-        out_host.copy_(x, non_blocking=True)
+        out_host.copy_(x_out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
     e2e_el = dist.max(time.perf_counter() - t0)
     e2e = {"value": job_rate(dist.world, args.steps, step_bytes, e2e_el), "unit": "GB/s",
@@ -441,10 +462,12 @@ def run_ours(args):
                    "frac_of_hbm_peak": value / dist.world / pk["hbm_gbs"],
                    "l2": f"inputs larger than L2: {step_bytes / 1e6:.0f} MB of weights per step, "
                          f"L2 {torch.cuda.get_device_properties(dev).L2_cache_size / 1e6:.0f} MB",
-                   "graph": f"one CUDA graph per step, {launches_per_layer * L} launches, programmatic dependent launch",
-                   "path": "fused (qg_decode_ffn_q8_0)" if fused else "unfused (4 launches per layer)",
+                   "graph": f"one CUDA graph per step, {launches_per_step} launches, programmatic dependent launch",
+                   "path": {"one": "one launch per layer (qg_decode_layer_q8_0: split-K down, cluster partials summed by the next layer) + finish",
+                            "two": "two launches per layer (qg_decode_ffn_q8_0)",
+                            "four": "four launches per layer (decode_ffn_q8_0)"}[path],
                    "parallelism": f"replicas x{dist.world} (independent decode streams, no collective)"},
-        "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_layer * L * args.steps, "clocks": clocks,
+        "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
     }
     if not args.quick:
         line["other_workloads"] = extra_configs(torch, pk)
@@ -508,7 +531,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layers", type=int, default=24)
     ap.add_argument("--quick", action="store_true", help="skip the other workloads' kernel rates")
-    ap.add_argument("--unfused", action="store_true", help="time the four-launch composition instead")
+    ap.add_argument("--path", choices=["one", "two", "four"], default="two",
+                    help="launches per decode layer: one (split-K down inside the layer kernel), two, four")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     if args.warmup < 3:

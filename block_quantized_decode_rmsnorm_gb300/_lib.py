@@ -27,6 +27,7 @@ SIGNATURES = {
     "qg_status_str": (ctypes.c_char_p, [ST]),
     "qg_abi_version": (I32, []),
     "qg_q8_0_pack": (ST, [P, I64, I64, P, P, P]),
+    "qg_q8_0_column_blocks": (ST, [P, P, I64, I64, P, P, P]),
     "quantize_act_q8_0": (ST, [P, I64, I64, P, P, P]),
     "qg_act_tiles_bytes": (I64, [I64, I64]),
     "quantize_act_q8_0_tiles": (ST, [P, I64, I64, P, P]),
@@ -37,6 +38,9 @@ SIGNATURES = {
     "qgemm_q8_0_prefill_tc": (ST, [P, P, I64, I64, P, I64, P, I32, P]),
     "qg_ffn_up_q8_0": (ST, [P, P, I64, F32, P, P, I64, P, P, P, P, P, P, P]),
     "qg_decode_ffn_q8_0": (ST, [P, P, I64, I64, F32, P, P, P, P, P, P, P, P]),
+    "qg_decode_layer_q8_0": (ST, [P, P, I32, P, P, P, I64, I64, F32, P, P, P, P, P, P, P, P]),
+    "qg_decode_layer_partials": (I32, [I64, I64]),
+    "qg_decode_layer_finish": (ST, [P, P, I32, I64, P, P]),
     "qg_debug_block_dots_q8_0": (ST, [P, I64, I64, P, I64, P, P]),
 }
 

@@ -267,6 +267,7 @@ class FFNLayer:
     gamma: torch.Tensor  # f32 [hidden]
     gate_up: Q8Weight    # [2*ffn, hidden]
     down: Q8Weight       # [hidden, ffn]
+    down_cb: "Q8Weight | None" = None  # down in the column-block layout (one-launch layer)
 
     @property
     def nbytes(self) -> int:
@@ -347,6 +348,95 @@ def qg_decode_ffn_q8_0(x: torch.Tensor, layer: FFNLayer, buf: FFNBuffers, eps: f
     _lib.call("qg_decode_ffn_q8_0", x.data_ptr(), layer.gamma.data_ptr(), hidden, ffn, float(eps),
               layer.gate_up.qs.data_ptr(), layer.gate_up.d.data_ptr(), layer.down.qs.data_ptr(),
               layer.down.d.data_ptr(), buf.h.data_ptr(), buf.hq.data_ptr(), buf.hd.data_ptr(), _stream_handle(stream))
+
+
+def qg_q8_0_column_blocks(w: Q8Weight, stream=None) -> Q8Weight:
+    """Row-major planes -> column-block planes: values [k/32, n, 32], scales [k/32, n]
+    (returned as a Q8Weight whose tensors have those shapes)."""
+    n, k = w.qs.shape
+    _need(w.qs, "w.qs", torch.int8, (n, k))
+    _need(w.d, "w.d", torch.float16, (n, k // 32))
+    out = Q8Weight(torch.empty((k // 32, n, 32), dtype=torch.int8, device=w.qs.device),
+                   torch.empty((k // 32, n), dtype=torch.float16, device=w.qs.device))
+    _lib.call("qg_q8_0_column_blocks", w.qs.data_ptr(), w.d.data_ptr(), n, k, out.qs.data_ptr(), out.d.data_ptr(),
+              _stream_handle(stream))
+    return out
+
+
+def prepare_one_launch(layer: FFNLayer) -> FFNLayer:
+    """Give the layer its down weights in the column-block layout (a one-time
+    load step; allocates, so do it before capturing a graph)."""
+    if layer.down_cb is None:
+        layer.down_cb = qg_q8_0_column_blocks(layer.down)
+    return layer
+
+
+def qg_decode_layer_partials(hidden: int, ffn: int) -> int:
+    n = _lib.load().qg_decode_layer_partials(hidden, ffn)
+    if n < 0:
+        raise ValueError(f"one-launch layer: unsupported shape hidden={hidden} ffn={ffn}")
+    return n
+
+
+def qg_decode_layer_q8_0(r_in: torch.Tensor, p_in: torch.Tensor | None, r_out: torch.Tensor, p_out: torch.Tensor,
+                         layer: FFNLayer, buf: FFNBuffers, eps: float = 1e-6, stream=None) -> None:
+    """One decode FFN layer in one launch on an unreduced input (r_in + rows of
+    p_in); writes its input as r_out and its output's partials to p_out."""
+    hidden = r_in.shape[-1]
+    ffn = layer.down.k
+    if layer.down_cb is None:
+        raise ValueError("qg_decode_layer_q8_0 needs layer.down_cb (see prepare_one_launch)")
+    _need(layer.down_cb.qs, "layer.down_cb.qs", torch.int8, (ffn // 32, hidden, 32))
+    _need(layer.down_cb.d, "layer.down_cb.d", torch.float16, (ffn // 32, hidden))
+    _need(r_in, "r_in", torch.float32, (hidden,))
+    _need(r_out, "r_out", torch.float32, (hidden,))
+    n_in = 0
+    if p_in is not None:
+        _need(p_in, "p_in", torch.float32)
+        n_in = p_in.shape[0]
+        _need(p_in, "p_in", torch.float32, (n_in, hidden))
+    _need(p_out, "p_out", torch.float32, (qg_decode_layer_partials(hidden, ffn), hidden))
+    _lib.call("qg_decode_layer_q8_0", r_in.data_ptr(), _ptr(p_in), n_in, r_out.data_ptr(), p_out.data_ptr(),
+              layer.gamma.data_ptr(), hidden, ffn, float(eps), layer.gate_up.qs.data_ptr(), layer.gate_up.d.data_ptr(),
+              layer.down_cb.qs.data_ptr(), layer.down_cb.d.data_ptr(), buf.h.data_ptr(), buf.hq.data_ptr(),
+              buf.hd.data_ptr(), _stream_handle(stream))
+
+
+def qg_decode_layer_finish(r: torch.Tensor, p: torch.Tensor | None, x: torch.Tensor | None = None,
+                           stream=None) -> torch.Tensor:
+    """x = r + sum of the rows of p, in row order."""
+    hidden = r.shape[-1]
+    _need(r, "r", torch.float32, (hidden,))
+    n = 0 if p is None else p.shape[0]
+    if p is not None:
+        _need(p, "p", torch.float32, (n, hidden))
+    if x is None:
+        x = torch.empty_like(r)
+    _need(x, "x", torch.float32, (hidden,))
+    _lib.call("qg_decode_layer_finish", r.data_ptr(), _ptr(p), n, hidden, x.data_ptr(), _stream_handle(stream))
+    return x
+
+
+class LayerStack:
+    """A stack of one-launch layers: two (r, partials) pairs used in turn, and
+    the output as one vector in `out` (r + partials of the last layer)."""
+
+    def __init__(self, hidden: int, ffn: int, device):
+        n = qg_decode_layer_partials(hidden, ffn)
+        self.r = [torch.zeros((hidden,), dtype=torch.float32, device=device) for _ in range(2)]
+        self.p = [torch.zeros((n, hidden), dtype=torch.float32, device=device) for _ in range(2)]
+        self.out = torch.zeros((hidden,), dtype=torch.float32, device=device)
+
+    def load(self, x: torch.Tensor) -> None:
+        self.r[0].copy_(x)
+
+    def run(self, layers, buf: FFNBuffers, eps: float = 1e-6, stream=None) -> torch.Tensor:
+        """Every layer (layer 0 reads r[0] alone), then the finish; returns `out`."""
+        for l, layer in enumerate(layers):
+            qg_decode_layer_q8_0(self.r[l % 2], self.p[l % 2] if l else None, self.r[(l + 1) % 2],
+                                 self.p[(l + 1) % 2], layer, buf, eps, stream=stream)
+        last = len(layers) % 2
+        return qg_decode_layer_finish(self.r[last], self.p[last] if layers else None, self.out, stream=stream)
 
 
 # --------------------------------------------------------------------------

@@ -10,6 +10,8 @@ cudaError_t launch_quantize_act(const float *, int64_t, int64_t, int8_t *, uint1
 cudaError_t launch_rmsnorm_quantize(const float *, const float *, int64_t, int64_t, float, int8_t *, uint16_t *,
                                     float *, cudaStream_t);
 cudaError_t launch_pack_q8_0(const void *, int64_t, int64_t, int8_t *, uint16_t *, cudaStream_t);
+cudaError_t launch_column_blocks(const int8_t *, const uint16_t *, int64_t, int64_t, int8_t *, uint16_t *,
+                                 cudaStream_t);
 cudaError_t launch_gemv_q8_0(const int8_t *, const uint16_t *, int64_t, int64_t, const int8_t *, const uint16_t *,
                              int64_t, int, const float *, float *, cudaStream_t);
 cudaError_t launch_block_dots(const int8_t *, int64_t, int64_t, const int8_t *, int64_t, int32_t *, cudaStream_t);
@@ -21,6 +23,13 @@ bool ffn_up_supported(int64_t k, int64_t half);
 cudaError_t launch_ffn_up(const float *, const float *, int64_t, float, const int8_t *, const uint16_t *, int64_t,
                           float *, int8_t *, uint16_t *, int8_t *, uint16_t *, float *, cudaStream_t);
 bool prefetch_supported(int64_t n_rows, int64_t k);
+bool decode_layer_supported(int64_t k, int64_t half);
+int decode_layer_partials(int64_t half);
+constexpr int kMaxLayerPartials = 16;
+cudaError_t launch_decode_layer(const float *, const float *, int, float *, float *, const float *, int64_t, float,
+                                const int8_t *, const uint16_t *, const int8_t *, const uint16_t *, int64_t, float *,
+                                int8_t *, uint16_t *, cudaStream_t);
+cudaError_t launch_layer_finish(const float *, const float *, int, int64_t, float *, cudaStream_t);
 cudaError_t launch_quantize_act_tiles(const float *, int64_t, int64_t, void *, cudaStream_t);
 bool prefill_tc_supported(int64_t k);
 cudaError_t launch_prefill_tc(const int8_t *, const uint16_t *, int64_t, int64_t, const void *, int64_t, float *, int,
@@ -52,6 +61,14 @@ constexpr int64_t kMaxK = int64_t(1) << 20;       // longest supported reduction
 constexpr int64_t kMaxRows = int64_t(1) << 31;    // rows per call
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// [a, a + na) and [b, b + nb) share a byte
+bool overlap(const void *a, size_t na, const void *b, size_t nb)
+{
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return na > 0 && nb > 0 && x < y + nb && y < x + na;
+}
+bool overlap(const void *a, const void *b, size_t bytes) { return overlap(a, bytes, b, bytes); }
 
 qg_status from_cuda(cudaError_t e)
 {
@@ -92,6 +109,19 @@ qg_status qg_q8_0_pack(const void *blocks, int64_t n_rows, int64_t k, int8_t *qs
     if (!blocks || !qs || !d) return QG_ERR_NULL;
     if (!aligned(qs, 32) || !aligned(d, 2)) return QG_ERR_ALIGN;
     return from_cuda(qg::launch_pack_q8_0(blocks, n_rows, k, qs, d, stream));
+}
+
+qg_status qg_q8_0_column_blocks(const int8_t *qs, const uint16_t *d, int64_t n_rows, int64_t k, int8_t *qs_cb,
+                                uint16_t *d_cb, qg_stream_t stream)
+{
+    if (n_rows < 0 || n_rows > kMaxRows) return QG_ERR_SHAPE;
+    if (qg_status st = check_q8_k(k); st != QG_OK) return st;
+    if (n_rows == 0) return QG_OK;
+    if (!qs || !d || !qs_cb || !d_cb) return QG_ERR_NULL;
+    if (!aligned(qs, 32) || !aligned(qs_cb, 32) || !aligned(d, 2) || !aligned(d_cb, 2)) return QG_ERR_ALIGN;
+    if (overlap(qs, qs_cb, static_cast<size_t>(n_rows) * k) || overlap(d, d_cb, static_cast<size_t>(n_rows) * (k / 32) * 2))
+        return QG_ERR_SHAPE;
+    return from_cuda(qg::launch_column_blocks(qs, d, n_rows, k, qs_cb, d_cb, stream));
 }
 
 qg_status quantize_act_q8_0(const float *x, int64_t rows, int64_t k, int8_t *q, uint16_t *d, qg_stream_t stream)
@@ -233,6 +263,53 @@ qg_status qg_decode_ffn_q8_0(float *x, const float *gamma, int64_t hidden, int64
         return from_cuda(qg::launch_gemv_prefetch(wdn_qs, wdn_d, hidden, ffn, hq, hd, QG_EPI_RESIDUAL_ADD, x, x,
                                                   stream));
     return from_cuda(qg::launch_gemv_q8_0(wdn_qs, wdn_d, hidden, ffn, hq, hd, 1, QG_EPI_RESIDUAL_ADD, x, x, stream));
+}
+
+static bool layer_shape_ok(int64_t hidden, int64_t ffn)
+{
+    return hidden > 0 && hidden % 32 == 0 && ffn > 0 && ffn % 32 == 0 && ffn <= kMaxRows / 2 && ffn <= kMaxK;
+}
+
+int32_t qg_decode_layer_partials(int64_t hidden, int64_t ffn)
+{
+    if (!layer_shape_ok(hidden, ffn) || !qg::decode_layer_supported(hidden, ffn)) return -1;
+    return qg::decode_layer_partials(ffn);
+}
+
+qg_status qg_decode_layer_q8_0(const float *r_in, const float *p_in, int32_t n_in, float *r_out, float *p_out,
+                               const float *gamma, int64_t hidden, int64_t ffn, float eps, const int8_t *wgu_qs,
+                               const uint16_t *wgu_d, const int8_t *wdn_qs, const uint16_t *wdn_d, float *h,
+                               int8_t *hq, uint16_t *hd, qg_stream_t stream)
+{
+    if (!layer_shape_ok(hidden, ffn)) return QG_ERR_SHAPE;
+    if (!(eps >= 0.0f) || n_in < 0 || n_in > qg::kMaxLayerPartials) return QG_ERR_SHAPE;
+    if (!qg::decode_layer_supported(hidden, ffn)) return QG_ERR_UNSUPPORTED;
+    if (!r_in || (n_in > 0 && !p_in) || !r_out || !p_out || !gamma || !wgu_qs || !wgu_d || !wdn_qs || !wdn_d || !h ||
+        !hq || !hd)
+        return QG_ERR_NULL;
+    if (!aligned(r_in, 16) || !aligned(p_in, 16) || !aligned(r_out, 16) || !aligned(p_out, 16) ||
+        !aligned(gamma, 16) || !aligned(wgu_qs, 32) || !aligned(wgu_d, 16) || !aligned(wdn_qs, 32) ||
+        !aligned(wdn_d, 16) || !aligned(h, 16) || !aligned(hq, 32) || !aligned(hd, 2))
+        return QG_ERR_ALIGN;
+    const size_t xb = static_cast<size_t>(hidden) * 4;
+    const size_t pin_b = xb * static_cast<size_t>(n_in);
+    const size_t pout_b = xb * static_cast<size_t>(qg::decode_layer_partials(ffn));
+    // the outputs are written while every CTA still reads the inputs
+    if (overlap(r_out, xb, r_in, xb) || overlap(p_out, pout_b, r_in, xb) || overlap(r_out, xb, p_in, pin_b) ||
+        overlap(p_out, pout_b, p_in, pin_b) || overlap(r_out, xb, p_out, pout_b))
+        return QG_ERR_SHAPE;
+    return from_cuda(qg::launch_decode_layer(r_in, p_in, n_in, r_out, p_out, gamma, hidden, eps, wgu_qs, wgu_d, wdn_qs,
+                                             wdn_d, ffn, h, hq, hd, stream));
+}
+
+qg_status qg_decode_layer_finish(const float *r, const float *p, int32_t n, int64_t hidden, float *x,
+                                 qg_stream_t stream)
+{
+    if (hidden < 0 || hidden > kMaxK || n < 0 || n > qg::kMaxLayerPartials) return QG_ERR_SHAPE;
+    if (hidden == 0) return QG_OK;
+    if (!r || (n > 0 && !p) || !x) return QG_ERR_NULL;
+    if (!aligned(r, 4) || !aligned(p, 4) || !aligned(x, 4)) return QG_ERR_ALIGN;
+    return from_cuda(qg::launch_layer_finish(r, p, n, hidden, x, stream));
 }
 
 qg_status qgemm_q8_0_prefill_tc(const int8_t *w_qs, const uint16_t *w_d, int64_t n_rows, int64_t k, const void *xt,

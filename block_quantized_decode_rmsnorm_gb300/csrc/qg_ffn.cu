@@ -30,6 +30,18 @@
 //    reads codes directly.
 //  * gemv_prefetch_kernel: batch-1 Q8_0 GEMV over pre-quantized input with the
 //    NONE or RESIDUAL epilogue (the down projection, and small GEMVs).
+//  * ffn_up_kernel<NBL, true>: the whole layer in one launch.  The down
+//    projection is split along its reduction: the CTA that owns block b of h
+//    also stages column block b of the down weights (hidden rows x 32 codes,
+//    contiguous in the column-block layout of qg_q8_0_column_blocks) and, once
+//    its h block is quantized, forms that block's Q8_0 term of every output.
+//    The CTAs of a thread-block cluster (up to 8) add their terms through
+//    distributed shared memory, each CTA one slice of the outputs, and every
+//    cluster stores its partial output vector.  The layer's output is left
+//    unreduced as (r, partials): the next layer (or qg_decode_layer_finish)
+//    forms x = r + sum of the partials in a fixed order while it loads its
+//    input anyway, so no float atomics and no extra pass are needed and the
+//    result is the same on every run.
 #include <mutex>
 
 #include "qg_common.cuh"
@@ -102,6 +114,8 @@ __device__ __forceinline__ float warp_sum_many(float (&v)[NV], int lane)
 // ---------------------------------------------------------------------------
 // gate|up with the norm in front and SiLU + quantization behind
 // ---------------------------------------------------------------------------
+constexpr int kMaxLayerPartials = 16;  // partial vectors a one-launch layer reads
+
 struct FfnUpParams {
     const float *x;       // [k] input row (written by the previous kernel)
     const float *gamma;   // [k]
@@ -118,13 +132,24 @@ struct FfnUpParams {
     int64_t half;         // F
     float inv_k;          // fl(1 / k)
     float eps;
+    // one-launch layer only (x above is r_in, the unreduced base of the input)
+    const float *p_in;         // [n_in][k] partials of the input (x = r_in + sum over them)
+    int n_in;
+    float *r_next;             // [k] this layer's input, x (written by CTA 0)
+    float *p_out;              // [F/32 / cluster][k] this layer's down partials, one per cluster
+    const int8_t *wdn_qs;      // down values, column-block layout [F/32][k][32]
+    const uint16_t *wdn_d;     // down scales, column-block layout [F/32][k]
+    int cluster;               // CTAs per cluster (divides F/32)
 };
 
-__host__ __device__ constexpr size_t ffn_up_smem_bytes(int k)
+__host__ __device__ constexpr size_t ffn_up_smem_bytes(int k, bool down = false)
 {
     // values [64][k] | scales [64][k/32] u16 | gamma [k] f32 | x codes [k] | x scales [k/32] f32
     // | h [32] f32 | warp partial pairs [2 * 16] f32
-    return static_cast<size_t>(64) * k + 64 * (k / 32) * 2 + 4 * k + k + 4 * (k / 32) + 4 * 32 + 4 * 32;
+    // | (one-launch layer) down column block [k][32] int8 | its scales [k] u16 | this CTA's
+    //   terms of every output [k] f32 | h codes [32] | h scale f32 (16 B)
+    return static_cast<size_t>(64) * k + 64 * (k / 32) * 2 + 4 * k + k + 4 * (k / 32) + 4 * 32 + 4 * 32 +
+           (down ? static_cast<size_t>(32) * k + 2 * k + 4 * k + 32 + 16 : 0);
 }
 
 // One CTA per 32-output block of h (rows o..o+31 of gate and of up).
@@ -136,7 +161,7 @@ __host__ __device__ constexpr size_t ffn_up_smem_bytes(int k)
 // threads quantize each 32-value block; the codes go through shared memory to
 // the lanes whose dot products read them (second barrier, which also covers
 // the staged weights).
-template <int NBL>
+template <int NBL, bool DOWN>
 __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
 {
     constexpr int OPW = 4 / NBL;  // outputs per warp
@@ -151,6 +176,11 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
     float *s_xd = reinterpret_cast<float *>(s_xq + K);
     float *s_h = s_xd + nb;
     float *s_part = s_h + 32;
+    int8_t *s_dn = reinterpret_cast<int8_t *>(s_part + 32);        // [K][32] (DOWN)
+    uint16_t *s_dnd = reinterpret_cast<uint16_t *>(s_dn + 32 * K);  // [K]     (DOWN)
+    float *s_out = reinterpret_cast<float *>(s_dnd + K);            // [K]     (DOWN)
+    int8_t *s_hq = reinterpret_cast<int8_t *>(s_out + K);           // [32]    (DOWN)
+    float *s_hd = reinterpret_cast<float *>(s_hq + 32);             // [1]     (DOWN)
 
     const int t = threadIdx.x;
     const int lane = t & 31;
@@ -170,8 +200,17 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
     if (warp == 0) {
         constexpr int PR = 8;  // rows per value piece
         const uint32_t sbytes = 64u * nb;
-        if (lane == 0) mbar_expect_tx(&s_bar, 4u * K + 2 * sbytes + 64u * K);
+        if (lane == 0) mbar_expect_tx(&s_bar, 4u * K + 2 * sbytes + 64u * K + (DOWN ? 34u * K : 0u));
         __syncwarp();
+        if (DOWN && lane >= 3 + 64 / PR && lane < 3 + 64 / PR + 5) {
+            // down column block b: four value pieces of K/4 rows x 32 bytes, then the K scales
+            const int v = lane - (3 + 64 / PR);
+            const int64_t cb = static_cast<int64_t>(blockIdx.x) * K;
+            void *dst = v < 4 ? static_cast<void *>(s_dn + v * 8 * K) : static_cast<void *>(s_dnd);
+            const void *src = v < 4 ? static_cast<const void *>(p.wdn_qs + (cb + v * (K / 4)) * QK)
+                                    : static_cast<const void *>(p.wdn_d + cb);
+            bulk_copy_g2s(dst, src, v < 4 ? 8u * K : 2u * K, &s_bar, l2_evict_first_policy());
+        }
         if (lane < 3 + 64 / PR) {
             const int v = lane - 3;                      // value piece: rows PR v .. of the stacked 64
             const int64_t vrow = (v < 32 / PR ? ob : p.half + ob - 32) + static_cast<int64_t>(PR) * v;
@@ -194,21 +233,44 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
     const bool live = 4 * t < K;
     float4 xv4 = make_float4(0.f, 0.f, 0.f, 0.f);
     if (live) xv4 = *reinterpret_cast<const float4 *>(p.x + 4 * t);
+    if constexpr (DOWN) {
+        // ... x = r + partials of the previous layer, all loads first, then the sum
+        // in partial order (the order qg_decode_layer_finish uses)
+        constexpr int MAXP = kMaxLayerPartials;
+        float4 pv[MAXP];
+#pragma unroll
+        for (int c = 0; c < MAXP; ++c)
+            if (c < p.n_in && live) pv[c] = *reinterpret_cast<const float4 *>(p.p_in + static_cast<int64_t>(c) * K + 4 * t);
+#pragma unroll
+        for (int c = 0; c < MAXP; ++c) {
+            if (c < p.n_in && live) {
+                xv4.x += pv[c].x;
+                xv4.y += pv[c].y;
+                xv4.z += pv[c].z;
+                xv4.w += pv[c].w;
+            }
+        }
+        if (blockIdx.x == 0 && live) *reinterpret_cast<float4 *>(p.r_next + 4 * t) = xv4;
+    }
+
 
     // ... then the staged slab (long since arrived, normally).  A copy that has
     // not landed within the limit leaves NaN outputs for this block.
-    if (!__syncthreads_and(mbar_wait_bounded(&s_bar, 0, kCopyWaitLimitNs))) {
+    const bool staged = __syncthreads_and(mbar_wait_bounded(&s_bar, 0, kCopyWaitLimitNs));
+    if (!staged) {
         if (warp == 0) {
             p.h[ob + lane] = __int_as_float(0x7fc00000);
             p.hq[ob + lane] = 0;
             if (lane == 0) p.hd[blockIdx.x] = 0x7e00;
         }
         mbar_wait_bounded(&s_bar, 0, kCopyWaitLimitNs);
-        return;
+        // the one-launch layer still takes part in its cluster's reduction (NaN terms)
+        if constexpr (!DOWN) return;
     }
+    const int c0 = lane_half(lane);
+    if (staged) {
     // While x is in flight, pull this warp's weight rows out of shared memory
     // into registers (rows: OPW gate rows, then OPW up rows).
-    const int c0 = lane_half(lane);
     u32x8 wr[NV][NBL];
     float wsc[NV][NBL];
 #pragma unroll
@@ -325,8 +387,52 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
         const float v = s_h[lane];
         const float m = warp_max(fabsf(v));
         const float dd = div127(m);
-        p.hq[ob + lane] = static_cast<int8_t>(q8_code(v, dd, __frcp_rn(dd)));
-        if (lane == 0) p.hd[blockIdx.x] = f2h_rn(dd);
+        const int8_t code = static_cast<int8_t>(q8_code(v, dd, __frcp_rn(dd)));
+        const uint16_t dbits = f2h_rn(dd);
+        p.hq[ob + lane] = code;
+        if (lane == 0) p.hd[blockIdx.x] = dbits;
+        if constexpr (DOWN) {
+            s_hq[lane] = code;
+            if (lane == 0) *s_hd = h2f(dbits);
+        }
+    }
+    }  // staged
+    if constexpr (DOWN) {
+        // ---- split-K down projection: block b's term of every output ---------
+        __syncthreads();  // h codes
+        constexpr int RPW_MAX = 128;  // rows per warp: K / (8 NBL) <= 128
+        const int rpw = K / NW;
+        const u32x8 hv = ld_block_halves(s_hq, c0);
+        const float dh = *s_hd;
+#pragma unroll
+        for (int i = 0; i < RPW_MAX / 32; ++i) {
+            if (32 * i + lane < rpw) {
+                const int row = warp * rpw + 32 * i + lane;
+                const u32x8 w = ld_block_halves(s_dn + row * QK, c0);
+                s_out[row] = staged ? block_term(w, hv, h2f(s_dnd[row]), dh, 0.0f) : __int_as_float(0x7fc00000);
+            }
+        }
+        // ---- cluster reduction through distributed shared memory ---------------
+        // CTA rank r sums outputs [r K / C, (r + 1) K / C) over the C CTAs of its
+        // cluster (loads first, then the sum in rank order) and stores the
+        // cluster's partial.
+        cluster_sync();  // every CTA's terms are complete
+        const int C = p.cluster;
+        const int slice = K / C;
+        const int r0 = static_cast<int>(cluster_ctarank()) * slice;
+        float *dst = p.p_out + static_cast<int64_t>(blockIdx.x / C) * K + r0;
+        for (int j = t; j < slice; j += blockDim.x) {
+            float v[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                if (c < C) v[c] = ld_cluster_f32(s_out + r0 + j, static_cast<uint32_t>(c));
+            float sum = v[0];
+#pragma unroll
+            for (int c = 1; c < 8; ++c)
+                if (c < C) sum += v[c];
+            dst[j] = sum;
+        }
+        cluster_sync();  // keep this CTA's terms alive until every reader is done
     }
 }
 
@@ -451,24 +557,39 @@ bool ffn_up_supported(int64_t k, int64_t half)
     return k % 256 == 0 && k <= 2048 && half % 32 == 0 && ffn_up_smem_bytes(static_cast<int>(k)) <= kMaxSmem;
 }
 
-template <int NBL>
+// One-launch layer: as above, and the down column slab must fit too; the
+// residual chunks of a CTA are at most four (k <= 128 * grid).
+// CTAs per cluster: the largest of 8, 4, 2, 1 that divides the grid.
+static unsigned layer_cluster(int64_t half)
+{
+    const int64_t grid = half / 32;
+    for (unsigned c : {8u, 4u, 2u})
+        if (grid % c == 0) return c;
+    return 1u;
+}
+
+bool decode_layer_supported(int64_t k, int64_t half)
+{
+    return ffn_up_supported(k, half) && ffn_up_smem_bytes(static_cast<int>(k), true) <= kMaxSmem &&
+           half / 32 / layer_cluster(half) <= kMaxLayerPartials;
+}
+
+template <int NBL, bool DOWN>
 static cudaError_t ffn_up_attr()
 {
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {
-        err = cudaFuncSetAttribute(ffn_up_kernel<NBL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        err = cudaFuncSetAttribute(ffn_up_kernel<NBL, DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    static_cast<int>(kMaxSmem));
     });
     return err;
 }
 
-cudaError_t launch_ffn_up(const float *x, const float *gamma, int64_t k, float eps, const int8_t *w_qs,
-                          const uint16_t *w_d, int64_t half, float *h, int8_t *hq, uint16_t *hd, int8_t *xq_out,
-                          uint16_t *xd_out, float *r_out, cudaStream_t s)
+static FfnUpParams ffn_up_params(const float *x, const float *gamma, int64_t k, float eps, const int8_t *w_qs,
+                                 const uint16_t *w_d, int64_t half, float *h, int8_t *hq, uint16_t *hd)
 {
-    if (half == 0) return cudaSuccess;
-    FfnUpParams p;
+    FfnUpParams p = {};
     p.x = x;
     p.gamma = gamma;
     p.w_qs = w_qs;
@@ -476,22 +597,61 @@ cudaError_t launch_ffn_up(const float *x, const float *gamma, int64_t k, float e
     p.h = h;
     p.hq = hq;
     p.hd = hd;
-    p.xq_out = xq_out;
-    p.xd_out = xd_out;
-    p.r_out = r_out;
     p.k = static_cast<int>(k);
     p.nb = static_cast<int>(k / QK);
     p.half = half;
     p.inv_k = 1.0f / static_cast<float>(k);
     p.eps = eps;
-    const dim3 grid(static_cast<unsigned>(half / 32));
-    const size_t smem = ffn_up_smem_bytes(p.k);
-    if (k <= 1024) {
-        if (cudaError_t e = ffn_up_attr<1>(); e != cudaSuccess) return e;
-        return launch_pdl(ffn_up_kernel<1>, grid, dim3(256), smem, s, p);
+    return p;
+}
+
+template <bool DOWN>
+static cudaError_t launch_ffn_up_impl(const FfnUpParams &p, cudaStream_t s)
+{
+    const dim3 grid(static_cast<unsigned>(p.half / 32));
+    const size_t smem = ffn_up_smem_bytes(p.k, DOWN);
+    const unsigned nbl = p.k <= 1024 ? 1 : 2;
+    if (nbl == 1) {
+        if (cudaError_t e = ffn_up_attr<1, DOWN>(); e != cudaSuccess) return e;
+    } else {
+        if (cudaError_t e = ffn_up_attr<2, DOWN>(); e != cudaSuccess) return e;
     }
-    if (cudaError_t e = ffn_up_attr<2>(); e != cudaSuccess) return e;
-    return launch_pdl(ffn_up_kernel<2>, grid, dim3(512), smem, s, p);
+    if constexpr (DOWN) {
+        if (nbl == 1) return launch_pdl_cluster(ffn_up_kernel<1, true>, grid, dim3(256), smem, s, p.cluster, p);
+        return launch_pdl_cluster(ffn_up_kernel<2, true>, grid, dim3(512), smem, s, p.cluster, p);
+    }
+    if (nbl == 1) return launch_pdl(ffn_up_kernel<1, DOWN>, grid, dim3(256), smem, s, p);
+    return launch_pdl(ffn_up_kernel<2, DOWN>, grid, dim3(512), smem, s, p);
+}
+
+cudaError_t launch_ffn_up(const float *x, const float *gamma, int64_t k, float eps, const int8_t *w_qs,
+                          const uint16_t *w_d, int64_t half, float *h, int8_t *hq, uint16_t *hd, int8_t *xq_out,
+                          uint16_t *xd_out, float *r_out, cudaStream_t s)
+{
+    if (half == 0) return cudaSuccess;
+    FfnUpParams p = ffn_up_params(x, gamma, k, eps, w_qs, w_d, half, h, hq, hd);
+    p.xq_out = xq_out;
+    p.xd_out = xd_out;
+    p.r_out = r_out;
+    return launch_ffn_up_impl<false>(p, s);
+}
+
+int decode_layer_partials(int64_t half) { return static_cast<int>(half / 32 / layer_cluster(half)); }
+
+cudaError_t launch_decode_layer(const float *r_in, const float *p_in, int n_in, float *r_out, float *p_out,
+                                const float *gamma, int64_t k, float eps, const int8_t *wgu_qs, const uint16_t *wgu_d,
+                                const int8_t *wdn_qs, const uint16_t *wdn_d, int64_t half, float *h, int8_t *hq,
+                                uint16_t *hd, cudaStream_t s)
+{
+    FfnUpParams p = ffn_up_params(r_in, gamma, k, eps, wgu_qs, wgu_d, half, h, hq, hd);
+    p.p_in = p_in;
+    p.n_in = n_in;
+    p.r_next = r_out;
+    p.p_out = p_out;
+    p.wdn_qs = wdn_qs;
+    p.wdn_d = wdn_d;
+    p.cluster = static_cast<int>(layer_cluster(half));
+    return launch_ffn_up_impl<true>(p, s);
 }
 
 // Rows per CTA when the rows are spread over one wave of num_sms CTAs.
@@ -556,6 +716,27 @@ cudaError_t launch_gemv_prefetch(const int8_t *w_qs, const uint16_t *w_d, int64_
     case 4: return launch_prefetch_nbl<4>(p, s);
     default: return cudaErrorInvalidValue;
     }
+}
+
+// x = r + sum of the partials, in partial order (the order the next layer's
+// prologue uses), for the output of a stack of one-launch layers.
+__global__ void __launch_bounds__(256) layer_finish_kernel(const float *__restrict__ r, const float *__restrict__ part,
+                                                           int n, int64_t k, float *__restrict__ x)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= k) return;
+    float v = r[i];
+    for (int c = 0; c < n; ++c) v += part[static_cast<int64_t>(c) * k + i];
+    x[i] = v;
+}
+
+cudaError_t launch_layer_finish(const float *r, const float *part, int n, int64_t k, float *x, cudaStream_t s)
+{
+    if (k == 0) return cudaSuccess;
+    return launch_pdl(layer_finish_kernel, dim3(static_cast<unsigned>((k + 255) / 256)), dim3(256), 0, s, r, part, n,
+                      k, x);
 }
 
 }  // namespace qg

@@ -147,6 +147,26 @@ __global__ void __launch_bounds__(256) pack_q8_0_kernel(const uint8_t *__restric
     dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
+// Row-major planes -> column-block-major planes: block b of row n moves to
+// qs_cb[b][n][0..31], its scale to d_cb[b][n], so the n_rows blocks of one
+// column block are contiguous.  One thread per block; like the pack above it
+// does not trigger its dependents early.
+__global__ void __launch_bounds__(256) column_blocks_kernel(const int8_t *__restrict__ qs,
+                                                            const uint16_t *__restrict__ d, int64_t n_rows, int nb,
+                                                            int8_t *__restrict__ qs_cb, uint16_t *__restrict__ d_cb)
+{
+    pdl_wait();
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;  // n * nb + b
+    if (i >= n_rows * nb) return;
+    const int64_t n = i / nb;
+    const int b = static_cast<int>(i - n * nb);
+    const uint4 *src = reinterpret_cast<const uint4 *>(qs + i * QK);
+    uint4 *dst = reinterpret_cast<uint4 *>(qs_cb + (static_cast<int64_t>(b) * n_rows + n) * QK);
+    dst[0] = src[0];
+    dst[1] = src[1];
+    d_cb[static_cast<int64_t>(b) * n_rows + n] = d[i];
+}
+
 // ---------------------------------------------------------------------------
 // Host launchers
 // ---------------------------------------------------------------------------
@@ -186,6 +206,16 @@ cudaError_t launch_pack_q8_0(const void *blocks, int64_t n_rows, int64_t k, int8
     const unsigned grid = static_cast<unsigned>((n_blocks + 255) / 256);
     return launch_pdl(pack_q8_0_kernel, dim3(grid), dim3(256), 0, s, static_cast<const uint8_t *>(blocks),
                       n_blocks, qs, d);
+}
+
+cudaError_t launch_column_blocks(const int8_t *qs, const uint16_t *d, int64_t n_rows, int64_t k, int8_t *qs_cb,
+                                 uint16_t *d_cb, cudaStream_t s)
+{
+    const int64_t n_blocks = n_rows * (k / QK);
+    if (n_blocks == 0) return cudaSuccess;
+    const unsigned grid = static_cast<unsigned>((n_blocks + 255) / 256);
+    return launch_pdl(column_blocks_kernel, dim3(grid), dim3(256), 0, s, qs, d, n_rows, static_cast<int>(k / QK), qs_cb,
+                      d_cb);
 }
 
 }  // namespace qg

@@ -94,6 +94,23 @@ QG_API qg_status qg_q8_0_pack(const void *blocks, int64_t n_rows, int64_t k,
                        int8_t *qs, uint16_t *d, qg_stream_t stream);
 
 /*
+ * qg_q8_0_column_blocks - re-lay packed Q8_0 planes column block by column
+ * block: block b of row n moves to qs_cb[b][n][0..31] and its scale to
+ * d_cb[b][n], so all rows of one 32-column block are contiguous.  The pages lay
+ * weights out for the kernel that reads them ([Phobos] GPU Performance
+ * Heisenbugs: groups of eight columns); this is the layout of the down weights
+ * of qg_decode_layer_q8_0, whose CTAs each read one column block of every row.
+ *   qs: device int8[n_rows][k] (read), 32-byte aligned; d: binary16 [n_rows][k/32]
+ *   qs_cb: device int8[k/32][n_rows][32] (written), 32-byte aligned
+ *   d_cb: device binary16 [k/32][n_rows] (written)
+ *   Outputs must not overlap inputs (QG_ERR_SHAPE).  A one-time load step; like
+ *   qg_q8_0_pack it does not let the next kernel start reading weights early.
+ */
+QG_API qg_status qg_q8_0_column_blocks(const int8_t *qs, const uint16_t *d, int64_t n_rows,
+                                       int64_t k, int8_t *qs_cb, uint16_t *d_cb,
+                                       qg_stream_t stream);
+
+/*
  * quantize_act_q8_0 - quantize activations to Q8_0, once, to be shared by
  * every projection that reads them ([Phobos] Fast Decode).
  * Per 32-value block: d = max|x| / 127 (f32), q = round half away from zero of
@@ -225,6 +242,61 @@ QG_API qg_status qg_decode_ffn_q8_0(float *x, const float *gamma, int64_t hidden
                                     float eps, const int8_t *wgu_qs, const uint16_t *wgu_d,
                                     const int8_t *wdn_qs, const uint16_t *wdn_d, float *h,
                                     int8_t *hq, uint16_t *hd, qg_stream_t stream);
+
+/*
+ * qg_decode_layer_q8_0 - one decode feed-forward block in ONE launch, its
+ * input and output each held unreduced as a base vector plus partial vectors:
+ *   x      = r_in + p_in[0] + ... + p_in[n_in - 1]        (f32, in that order)
+ *   r_out  = x
+ *   r_out + p_out[0] + ... + p_out[P - 1] = x + down(Q8_0(SiLU(g) * u)),
+ *   (g|u)  = gate|up(Q8_0(RMSNorm(x) * gamma)),  P = qg_decode_layer_partials.
+ * [Phobos] Fast Decode: quantize once and share, stack the projections, fold
+ * the residual into the matmul; [Herbert] Emitting for a GPU: fuse the
+ * normalization and the activation with the projections around them.  The
+ * pages launch the down projection separately; here it is split along its
+ * reduction: the CTA that produces block b of h forms that block's Q8_0 term
+ * of every output (f32(d_w[n][b]) * f32(d_h[b]) * exact block sum), the CTAs
+ * of a thread-block cluster (up to 8) add their terms on chip, and each
+ * cluster stores one partial output vector.  The next layer sums them while
+ * it loads its input, so no pass over the output and no atomics are needed;
+ * every sum is in a fixed order, so results repeat bit for bit.
+ *   r_in:  device f32[hidden] (read), 16-byte aligned
+ *   p_in:  device f32[n_in][hidden] (read), 16-byte aligned; NULL when n_in = 0;
+ *          n_in <= 16
+ *   r_out: device f32[hidden] (written), 16-byte aligned
+ *   p_out: device f32[P][hidden] (written), 16-byte aligned
+ *          No output may overlap an input or the other output (QG_ERR_SHAPE).
+ *   gamma, wgu_*, h, hq, hd: as qg_decode_ffn_q8_0 (h, hq, hd left holding
+ *          this block's activation).
+ *   wdn_qs, wdn_d: the down weights in the column-block layout written by
+ *          qg_q8_0_column_blocks: values int8[ffn/32][hidden][32] (32-byte
+ *          aligned), scales binary16[ffn/32][hidden] (16-byte aligned).
+ *   hidden a multiple of 256 whose one-launch working set fits one CTA's shared
+ *   memory (hidden <= 1792 on GB300); ffn a multiple of 32 with P <= 16
+ *   (QG_ERR_UNSUPPORTED otherwise).  A CTA whose staged copies stall beyond
+ *   one second contributes NaN instead of hanging.
+ * A stack of layers ping-pongs two (r, p) pairs, layer 0 with n_in = 0, and
+ * ends with qg_decode_layer_finish.
+ */
+QG_API qg_status qg_decode_layer_q8_0(const float *r_in, const float *p_in, int32_t n_in,
+                                      float *r_out, float *p_out, const float *gamma,
+                                      int64_t hidden, int64_t ffn, float eps,
+                                      const int8_t *wgu_qs, const uint16_t *wgu_d,
+                                      const int8_t *wdn_qs, const uint16_t *wdn_d, float *h,
+                                      int8_t *hq, uint16_t *hd, qg_stream_t stream);
+
+/* Partial vectors P a qg_decode_layer_q8_0 call writes (-1: shape unsupported). */
+QG_API int32_t qg_decode_layer_partials(int64_t hidden, int64_t ffn);
+
+/*
+ * qg_decode_layer_finish - x = r + p[0] + ... + p[n - 1] (f32, in that order,
+ * the order the next layer would use): the output of a stack of one-launch
+ * layers as one vector.
+ *   r: device f32[hidden]; p: device f32[n][hidden] (NULL when n = 0), n <= 16;
+ *   x: device f32[hidden] (written; may be r itself).
+ */
+QG_API qg_status qg_decode_layer_finish(const float *r, const float *p, int32_t n, int64_t hidden,
+                                        float *x, qg_stream_t stream);
 
 /*
  * qgemm_q8_0_prefill_tc - the prompt contraction of qgemm_q8_0_prefill on the

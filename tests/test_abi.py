@@ -142,3 +142,32 @@ def test_act_tiles_size_and_errors(lib):
     assert qt(FAKE, 1, 64, FAKE + 8, None) == 2
     assert qt(None, 1, 64, FAKE, None) == 1
     assert qt(None, 0, 64, None, None) == 0
+
+
+def test_one_launch_layer_argument_errors(lib):
+    f = lib.qg_decode_layer_q8_0
+    eps = ctypes.c_float(1e-6)
+    xb, pb = 4096, 14 * 4096
+    RI, PI, RO, PO = FAKE, FAKE + xb, FAKE + xb + pb, FAKE + 2 * xb + pb
+    args = lambda ri, pi, n, ro, po, hidden=1024, ffn=3584: (ri, pi, n, ro, po, FAKE, hidden, ffn, eps, FAKE, FAKE,
+                                                             FAKE, FAKE, FAKE, FAKE, FAKE, None)
+    assert lib.qg_decode_layer_partials(1024, 3584) == 14
+    assert lib.qg_decode_layer_partials(256, 96) == 3
+    assert lib.qg_decode_layer_partials(2048, 1024) == -1
+    # working set beyond a CTA's shared memory, hidden not a multiple of 256, too many partials
+    assert f(*args(RI, PI, 14, RO, PO, 2048, 1024)) == 4
+    assert f(*args(RI, PI, 14, RO, PO, 992, 3584)) == 4
+    assert f(*args(RI, PI, 14, RO, PO, 1024, 32 * 8 * 17)) == 4
+    assert f(*args(RI, PI, 17, RO, PO)) == 3
+    # outputs overlapping inputs or each other
+    assert f(*args(RI, PI, 14, RI, PO)) == 3
+    assert f(*args(RI, PI, 14, RO, PI + 4096)) == 3
+    assert f(*args(RI, PI, 14, RO, RO)) == 3
+    # alignment, null partials with n_in > 0, null output
+    assert f(*args(RI + 4, PI, 14, RO, PO)) == 2
+    assert f(*args(RI, None, 14, RO, PO)) == 1
+    assert f(*args(RI, PI, 14, None, PO)) == 1
+    fin = lib.qg_decode_layer_finish
+    assert fin(FAKE, FAKE, 17, 1024, FAKE, None) == 3
+    assert fin(FAKE, None, 2, 1024, FAKE, None) == 1
+    assert fin(None, None, 0, 0, None, None) == 0
