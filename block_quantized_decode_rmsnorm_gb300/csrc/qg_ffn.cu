@@ -81,35 +81,6 @@ __device__ __forceinline__ u32x8 ld_block_halves(const int8_t *p, int c0)
 
 __device__ __forceinline__ int lane_half(int lane) { return (lane >> 2) & 1; }
 
-// Sum NV per-lane partials across the warp in one butterfly: at offset 16 a lane
-// keeps half of its values and receives the partner's other half, and so on, so
-// NV values need NV - 1 + (5 - log2 NV) shuffles instead of 5 NV.  Every value
-// is summed over the same lane pairs, in the same order, as warp_sum does.
-// Returns the total of value index  sum over the first log2(NV) offsets o of
-// (lane & o ? NV/2^(step+1) : 0).
-template <int NV>
-__device__ __forceinline__ float warp_sum_many(float (&v)[NV], int lane)
-{
-    int n = NV;
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-        if (n > 1) {
-            const bool upper = (lane & off) != 0;
-#pragma unroll
-            for (int k = 0; k < NV / 2; ++k) {
-                if (k < n / 2) {
-                    const float send = upper ? v[k] : v[k + n / 2];
-                    const float keep = upper ? v[k + n / 2] : v[k];
-                    v[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-                }
-            }
-            n /= 2;
-        } else {
-            v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
-        }
-    }
-    return v[0];
-}
 
 // ---------------------------------------------------------------------------
 // gate|up with the norm in front and SiLU + quantization behind

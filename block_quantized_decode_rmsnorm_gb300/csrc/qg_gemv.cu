@@ -59,25 +59,45 @@ __device__ __forceinline__ int64_t slot_row(const GemvParams &p, int64_t t, int 
 template <int B, int R>
 __device__ __forceinline__ void reduce_and_store(const GemvParams &p, int64_t t, int lane, float (&acc)[R][B])
 {
+    // All R*B sums in one transposed butterfly (R*B - 1 + 5 - log2(R*B)
+    // shuffles, the same pairings and order as one warp_sum per value): lane l
+    // ends with value v = l >> SH, v = s * B + b.
+    // (Batch 2 keeps one warp_sum per value: the butterfly's extra live values
+    // cost it registers, and so resident warps, that the few shuffles saved do
+    // not pay for.  Both give the same bits.)
+    constexpr int NV = R * B;
+    constexpr bool MANY = B != 2;
+    constexpr int SH = !MANY ? 0 : NV >= 32 ? 0 : NV >= 16 ? 1 : NV >= 8 ? 2 : NV >= 4 ? 3 : NV >= 2 ? 4 : 5;
     float val = 0.0f;
+    if constexpr (MANY) {
+        float v[NV];
 #pragma unroll
-    for (int s = 0; s < R; ++s)
+        for (int s = 0; s < R; ++s)
 #pragma unroll
-        for (int b = 0; b < B; ++b) {
-            const float v = warp_sum(acc[s][b]);
-            if (lane == s * B + b) val = v;
-        }
-    const int s = lane / B;
-    const int b = lane % B;
+            for (int b = 0; b < B; ++b) v[s * B + b] = acc[s][b];
+        val = warp_sum_many<NV>(v, lane);
+    } else {
+#pragma unroll
+        for (int s = 0; s < R; ++s)
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const float w = warp_sum(acc[s][b]);
+                if (lane == s * B + b) val = w;
+            }
+    }
+    const int idx = lane >> SH;
+    const bool rep = !MANY ? idx < NV : (lane & ((1 << SH) - 1)) == 0;  // one lane per value stores it
+    const int s = idx / B;
+    const int b = idx % B;
     if (p.epi == QG_EPI_SILU_MUL_HALVES) {
-        const float u = __shfl_down_sync(0xffffffffu, val, B);  // slot s+1 = up row of the pair
-        if (lane < R * B && (s & 1) == 0 && b < p.batch) {
+        const float u = __shfl_down_sync(0xffffffffu, val, B << SH);  // slot s+1 = up row of the pair
+        if (rep && (s & 1) == 0 && b < p.batch) {
             const int64_t o = t * (R / 2) + (s >> 1);
             if (o < p.half) p.y[b * p.n_out + o] = silu_mul(val, u);
         }
         return;
     }
-    if (lane < R * B && b < p.batch) {
+    if (rep && b < p.batch) {
         const int64_t row = t * R + s;
         if (row < p.n_rows) {
             float out = val;
