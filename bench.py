@@ -478,6 +478,52 @@ def run_ours(args):
     dist.close()
 
 
+def run_workload(args):
+    """One workload's kernel alone, launched eagerly warmup + steps times (for
+    profiling one kernel, e.g. under ncu); prints its mean launch time."""
+    import torch
+
+    from block_quantized_decode_rmsnorm_gb300 import api, build, synth
+
+    torch.cuda.set_device(0)
+    build()
+    w = args.workload
+    if w == "prefill":
+        pc = synth.prefill_case(0)
+        wt = api.q8_weight_from_numpy(pc["w_qs"], pc["w_d"])
+        xt = api.quantize_act_q8_0_tiles(torch.from_numpy(pc["x"]).cuda())
+        y = torch.empty((pc["x"].shape[0], pc["w_qs"].shape[0]), dtype=torch.float32, device="cuda")
+        fn = lambda: api.qgemm_q8_0_prefill_tc(wt, xt, y=y)
+        name = "prompt contraction 512x7168x1024, tcgen05"
+    elif w.startswith("head"):
+        b = int(w[4:])
+        qs, d = synth.q8_0_weight_planes(0, synth.S_W0, 262144, 1024)
+        wt = api.q8_weight_from_numpy(qs, d)
+        xq, xd = api.quantize_act_q8_0(torch.from_numpy(synth.f32_normal(0, synth.S_X, (b, 1024))).cuda())
+        y = torch.empty((b, 262144), dtype=torch.float32, device="cuda")
+        fn = lambda: api.qgemv_q8_0(wt, xq, xd, y=y)
+        name = f"output head 262144x1024, batch {b}"
+    else:  # bf16
+        bc = synth.bf16_case(0)
+        wb, xb, gb = api.bf16_from_bits(bc["w"]), api.bf16_from_bits(bc["x"]), api.bf16_from_bits(bc["gamma"])
+        y = torch.empty((bc["w"].shape[0] // 2,), dtype=torch.float32, device="cuda")
+        fn = lambda: api.qgemv_bf16(wb, xb, gb, EPS, epilogue="silu_mul", y=y)
+        name = "bf16 gate|up 18432x2560 + RMSNorm + SiLU*u"
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"workload": name, "launches": args.steps,
+                      "us_per_launch": e0.elapsed_time(e1) * 1e3 / args.steps,
+                      "note": "eager back-to-back launches of one kernel, warm L2; for profiling, not the bench line"}),
+          flush=True)
+
+
 def run_reference(args):
     """The CPU oracle as the reference arm: same workload, metric and unit."""
     rank = int(os.environ.get("RANK", "0"))
@@ -534,11 +580,15 @@ def main():
     ap.add_argument("--path", choices=["one", "two", "four"], default="two",
                     help="launches per decode layer: one (split-K down inside the layer kernel), two, four")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--workload", choices=["prefill", "head1", "head2", "head4", "head8", "bf16"],
+                    help="time one workload's kernel alone (for profiling) instead of the bench step")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload:
+        run_workload(args)
     else:
         run_ours(args)
 
