@@ -439,6 +439,33 @@ class LayerStack:
         return qg_decode_layer_finish(self.r[last], self.p[last] if layers else None, self.out, stream=stream)
 
 
+def qg_decode_layers_q8_0_noalloc(x_in: torch.Tensor, layers, eps: float = 1e-6, x_out: torch.Tensor | None = None,
+                                  stream=None) -> torch.Tensor:
+    """A stack of one-launch layers with the library's fixed scratch array instead
+    of caller work buffers (layers need down_cb, see prepare_one_launch)."""
+    import ctypes
+
+    hidden = x_in.shape[-1]
+    _need(x_in, "x_in", torch.float32, (hidden,))
+    if x_out is None:
+        x_out = torch.empty_like(x_in)
+    _need(x_out, "x_out", torch.float32, (hidden,))
+    n = len(layers)
+    ffn = layers[0].down.k if n else 0
+    for ly in layers:
+        if ly.down_cb is None:
+            raise ValueError("qg_decode_layers_q8_0_noalloc needs down_cb on every layer (see prepare_one_launch)")
+    arr = lambda vals: (ctypes.c_void_p * max(n, 1))(*vals) if n else None
+    g = arr([ly.gamma.data_ptr() for ly in layers])
+    gq = arr([ly.gate_up.qs.data_ptr() for ly in layers])
+    gd = arr([ly.gate_up.d.data_ptr() for ly in layers])
+    dq = arr([ly.down_cb.qs.data_ptr() for ly in layers])
+    dd = arr([ly.down_cb.d.data_ptr() for ly in layers])
+    _lib.call("qg_decode_layers_q8_0_noalloc", x_in.data_ptr(), x_out.data_ptr(), n, g, gq, gd, dq, dd, hidden,
+              ffn if n else 32, float(eps), _stream_handle(stream))
+    return x_out
+
+
 # --------------------------------------------------------------------------
 # host <-> device helpers (plumbing)
 # --------------------------------------------------------------------------

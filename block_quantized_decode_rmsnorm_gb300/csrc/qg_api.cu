@@ -30,6 +30,11 @@ cudaError_t launch_decode_layer(const float *, const float *, int, float *, floa
                                 const int8_t *, const uint16_t *, const int8_t *, const uint16_t *, int64_t, float *,
                                 int8_t *, uint16_t *, cudaStream_t);
 cudaError_t launch_layer_finish(const float *, const float *, int, int64_t, float *, cudaStream_t);
+size_t layer_scratch_bytes(int64_t hidden, int64_t ffn, int partials);
+size_t layer_scratch_capacity();
+cudaError_t launch_decode_layers_noalloc(const float *, float *, int, const float *const *, const int8_t *const *,
+                                         const uint16_t *const *, const int8_t *const *, const uint16_t *const *,
+                                         int64_t, int64_t, float, cudaStream_t);
 cudaError_t launch_quantize_act_tiles(const float *, int64_t, int64_t, void *, cudaStream_t);
 bool prefill_tc_supported(int64_t k);
 cudaError_t launch_prefill_tc(const int8_t *, const uint16_t *, int64_t, int64_t, const void *, int64_t, float *, int,
@@ -310,6 +315,28 @@ qg_status qg_decode_layer_finish(const float *r, const float *p, int32_t n, int6
     if (!r || (n > 0 && !p) || !x) return QG_ERR_NULL;
     if (!aligned(r, 4) || !aligned(p, 4) || !aligned(x, 4)) return QG_ERR_ALIGN;
     return from_cuda(qg::launch_layer_finish(r, p, n, hidden, x, stream));
+}
+
+qg_status qg_decode_layers_q8_0_noalloc(const float *x_in, float *x_out, int32_t n_layers, const float *const *gamma,
+                                       const int8_t *const *wgu_qs, const uint16_t *const *wgu_d,
+                                       const int8_t *const *wdn_qs, const uint16_t *const *wdn_d, int64_t hidden,
+                                       int64_t ffn, float eps, qg_stream_t stream)
+{
+    if (!layer_shape_ok(hidden, ffn) || n_layers < 0 || n_layers > 65536 || !(eps >= 0.0f)) return QG_ERR_SHAPE;
+    if (!qg::decode_layer_supported(hidden, ffn)) return QG_ERR_UNSUPPORTED;
+    if (qg::layer_scratch_bytes(hidden, ffn, qg::decode_layer_partials(ffn)) > qg::layer_scratch_capacity())
+        return QG_ERR_UNSUPPORTED;  // the fixed scratch array is too small for this shape
+    if (!x_in || !x_out) return QG_ERR_NULL;
+    if (n_layers > 0 && (!gamma || !wgu_qs || !wgu_d || !wdn_qs || !wdn_d)) return QG_ERR_NULL;
+    if (!aligned(x_in, 16) || !aligned(x_out, 4)) return QG_ERR_ALIGN;
+    for (int32_t l = 0; l < n_layers; ++l) {
+        if (!gamma[l] || !wgu_qs[l] || !wgu_d[l] || !wdn_qs[l] || !wdn_d[l]) return QG_ERR_NULL;
+        if (!aligned(gamma[l], 16) || !aligned(wgu_qs[l], 32) || !aligned(wgu_d[l], 16) || !aligned(wdn_qs[l], 32) ||
+            !aligned(wdn_d[l], 16))
+            return QG_ERR_ALIGN;
+    }
+    return from_cuda(qg::launch_decode_layers_noalloc(x_in, x_out, n_layers, gamma, wgu_qs, wgu_d, wdn_qs, wdn_d,
+                                                      hidden, ffn, eps, stream));
 }
 
 qg_status qgemm_q8_0_prefill_tc(const int8_t *w_qs, const uint16_t *w_d, int64_t n_rows, int64_t k, const void *xt,

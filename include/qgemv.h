@@ -299,6 +299,36 @@ QG_API qg_status qg_decode_layer_finish(const float *r, const float *p, int32_t 
                                         float *x, qg_stream_t stream);
 
 /*
+ * qg_decode_layers_q8_0_noalloc - a stack of n_layers one-launch decode layers
+ * (qg_decode_layer_q8_0 for each, then qg_decode_layer_finish into x_out) that
+ * needs no caller-provided work memory.  The pages have no counterpart: this
+ * entry point exists for callers that cannot allocate device memory.  The
+ * layers' intermediates (the unreduced inputs and outputs, h and its codes)
+ * live in one fixed array compiled into the library, 256 KB per GPU; shapes
+ * whose intermediates do not fit it are refused with QG_ERR_UNSUPPORTED
+ * (hidden 1024 / ffn 3584 needs 141,056 bytes; hidden 1792 / ffn 4096 does
+ * not fit).  Results are the same bits as
+ * running the layers through qg_decode_layer_q8_0 with caller buffers.
+ *   x_in:  device f32[hidden] (read), 16-byte aligned
+ *   x_out: device f32[hidden] (written); may be x_in
+ *   gamma, wgu_qs, wgu_d, wdn_qs, wdn_d: HOST arrays of n_layers DEVICE
+ *          pointers, one set per layer, as qg_decode_layer_q8_0 (down weights
+ *          in the column-block layout of qg_q8_0_column_blocks); read during
+ *          the call only.
+ *   hidden, ffn, eps: as qg_decode_layer_q8_0, the same for every layer.
+ * Concurrency: the array is shared by every call on a GPU, so calls on the same
+ * GPU must not overlap in time (one stream, or synchronise between them).
+ * The first call on each GPU looks the array up (a host-side query): make it
+ * before capturing the call into a CUDA graph.
+ */
+QG_API qg_status qg_decode_layers_q8_0_noalloc(const float *x_in, float *x_out, int32_t n_layers,
+                                               const float *const *gamma,
+                                               const int8_t *const *wgu_qs, const uint16_t *const *wgu_d,
+                                               const int8_t *const *wdn_qs, const uint16_t *const *wdn_d,
+                                               int64_t hidden, int64_t ffn, float eps,
+                                               qg_stream_t stream);
+
+/*
  * qgemm_q8_0_prefill_tc - the prompt contraction of qgemm_q8_0_prefill on the
  * tcgen05 tensor cores ([Phobos] Fast Decode: prompt processing belongs on the
  * tensor cores; GPU Performance Heisenbugs: exact integer values on the tensor

@@ -171,3 +171,20 @@ def test_one_launch_layer_argument_errors(lib):
     assert fin(FAKE, FAKE, 17, 1024, FAKE, None) == 3
     assert fin(FAKE, None, 2, 1024, FAKE, None) == 1
     assert fin(None, None, 0, 0, None, None) == 0
+
+
+def test_noalloc_stack_argument_errors(lib):
+    f = lib.qg_decode_layers_q8_0_noalloc
+    eps = ctypes.c_float(1e-6)
+    arr = (ctypes.c_void_p * 1)(FAKE)
+    # intermediates larger than the fixed scratch array: refused before any launch
+    assert f(FAKE, FAKE, 1, arr, arr, arr, arr, arr, 1792, 4096, eps, None) == 4
+    # unsupported layer shape, negative count
+    assert f(FAKE, FAKE, 1, arr, arr, arr, arr, arr, 2048, 1024, eps, None) == 4
+    assert f(FAKE, FAKE, -1, arr, arr, arr, arr, arr, 1024, 3584, eps, None) == 3
+    # null pointer arrays / entries, misaligned input
+    assert f(FAKE, FAKE, 1, None, arr, arr, arr, arr, 1024, 3584, eps, None) == 1
+    nul = (ctypes.c_void_p * 1)(None)
+    assert f(FAKE, FAKE, 1, arr, nul, arr, arr, arr, 1024, 3584, eps, None) == 1
+    assert f(FAKE + 4, FAKE, 1, arr, arr, arr, arr, arr, 1024, 3584, eps, None) == 2
+    assert f(None, FAKE, 0, None, None, None, None, None, 1024, 3584, eps, None) == 1
