@@ -186,6 +186,115 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_q8_0_reg_kernel(const GemvP
 #undef QG_LOAD_WEIGHTS
 }
 
+// ---------------------------------------------------------------------------
+// Batched GEMV on the int8 tensor cores (batch 3..8, K a multiple of 256)
+// ---------------------------------------------------------------------------
+// "Filling in the blanks: Inference using Phobos", GPU Performance Heisenbugs:
+// exact int8 values on the integer tensor cores.  One mma.sync.m16n8k32 (s8,
+// s32 accumulate) is exactly one 32-value block of 16 weight rows against the
+// batch (N = 8, unused columns zero), so the block sums come out exact and the
+// scales d_w d_x are applied per block as in the dp4a kernel.  A warp owns 16
+// rows per task; thread (g = lane / 4, t = lane % 4) loads 8 bytes of rows g
+// and g + 8 per block straight from HBM (the four threads of a row cover its
+// 32 bytes) and the batch's codes come from shared memory, staged once per CTA.
+// The fragment positions of K inside a block are permuted the same way for both
+// operands (thread t carries values 8t..8t+7), which leaves every block sum
+// unchanged.  With the activations out of registers a thread needs about 70
+// registers, so many more warps (and weight bytes) are in flight than in the
+// register-tile kernel at the same batch.
+constexpr int MMA_ROWS = 16;
+constexpr int MMA_GROUP = 8;  // blocks of weights requested together per thread
+
+__device__ __forceinline__ uint2 ld_stream_8B(const void *p)
+{
+    uint2 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void mma_s8_16832(int (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+r"(c[0]), "+r"(c[1]), "+r"(c[2]), "+r"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__global__ void __launch_bounds__(GEMV_THREADS) gemv_q8_0_mma_kernel(const GemvParams p)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int K = p.k, nb = p.nb;
+    const int XS = K + 32;  // row stride of the staged codes: conflict-free 8-byte fragment loads
+    int8_t *s_x = reinterpret_cast<int8_t *>(smem);
+    float *s_xd = reinterpret_cast<float *>(smem + 8 * XS);  // [8][nb]
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int wpc = blockDim.x >> 5;
+    const int64_t n_tasks = (p.n_rows + MMA_ROWS - 1) / MMA_ROWS;
+
+    pdl_trigger();
+    pdl_wait();
+    // batch codes and scales, rows past the batch zero
+    for (int i = threadIdx.x; i < 8 * (K / 16); i += blockDim.x) {
+        const int b = i / (K / 16), off = (i - b * (K / 16)) * 16;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (b < p.batch) v = ld_16B(p.xq + static_cast<int64_t>(b) * K + off);
+        *reinterpret_cast<uint4 *>(s_x + b * XS + off) = v;
+    }
+    for (int i = threadIdx.x; i < 8 * nb; i += blockDim.x) {
+        const int b = i / nb;
+        s_xd[i] = b < p.batch ? h2f(p.xd[i]) : 0.0f;
+    }
+    __syncthreads();
+
+    for (int64_t task = static_cast<int64_t>(blockIdx.x) * wpc + (threadIdx.x >> 5); task < n_tasks;
+         task += static_cast<int64_t>(gridDim.x) * wpc) {
+        const int64_t rA = task * MMA_ROWS + g, rB = rA + 8;
+        const bool vA = rA < p.n_rows, vB = rB < p.n_rows;
+        const int8_t *wA = p.w_qs + rA * K + 8 * t;
+        const int8_t *wB = p.w_qs + rB * K + 8 * t;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};  // (row g, batch 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1)
+        for (int j0 = 0; j0 < nb; j0 += MMA_GROUP) {
+            uint2 a[MMA_GROUP], b[MMA_GROUP];
+#pragma unroll
+            for (int u = 0; u < MMA_GROUP; ++u) {
+                a[u] = vA ? ld_stream_8B(wA + (j0 + u) * QK) : make_uint2(0u, 0u);
+                b[u] = vB ? ld_stream_8B(wB + (j0 + u) * QK) : make_uint2(0u, 0u);
+            }
+            // the eight blocks' scales of rows g and g + 8: 16 bytes each
+            uint4 dA = make_uint4(0u, 0u, 0u, 0u), dB = make_uint4(0u, 0u, 0u, 0u);
+            if (vA) dA = ld_nc_16B(p.w_d + rA * nb + j0);
+            if (vB) dB = ld_nc_16B(p.w_d + rB * nb + j0);
+            const uint16_t *sdA = reinterpret_cast<const uint16_t *>(&dA);
+            const uint16_t *sdB = reinterpret_cast<const uint16_t *>(&dB);
+#pragma unroll
+            for (int u = 0; u < MMA_GROUP; ++u) {
+                const int blk = j0 + u;
+                const uint2 xf = *reinterpret_cast<const uint2 *>(s_x + g * XS + blk * QK + 8 * t);
+                int c[4] = {0, 0, 0, 0};
+                mma_s8_16832(c, a[u].x, b[u].x, a[u].y, b[u].y, xf.x, xf.y);
+                const float x0 = s_xd[(2 * t) * nb + blk], x1 = s_xd[(2 * t + 1) * nb + blk];
+                const float wa = h2f(sdA[u]), wb = h2f(sdB[u]);
+                acc[0] = fmaf(small_int_to_float(c[0]), wa * x0, acc[0]);
+                acc[1] = fmaf(small_int_to_float(c[1]), wa * x1, acc[1]);
+                acc[2] = fmaf(small_int_to_float(c[2]), wb * x0, acc[2]);
+                acc[3] = fmaf(small_int_to_float(c[3]), wb * x1, acc[3]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t row = (i < 2) ? rA : rB;
+            const int bcol = 2 * t + (i & 1);
+            if (row < p.n_rows && bcol < p.batch) {
+                float out = acc[i];
+                if (p.epi == QG_EPI_RESIDUAL_ADD) out = p.residual[bcol * p.n_rows + row] + out;
+                p.y[bcol * p.n_out + row] = out;
+            }
+        }
+    }
+}
+
 // Generic path: any nb; activation read through L1 per block.
 template <int B, int R>
 __global__ void __launch_bounds__(GEMV_THREADS) gemv_q8_0_generic_kernel(const GemvParams p)
@@ -270,16 +379,16 @@ __global__ void __launch_bounds__(256) block_dots_kernel(const int8_t *__restric
 // Host side
 // ---------------------------------------------------------------------------
 // Resident CTAs per SM of one kernel, cached per kernel (function pointer).
-static int max_ctas_per_sm(const void *kernel)
+static int max_ctas_per_sm(const void *kernel, size_t smem = 0)
 {
     static std::mutex mu;
-    static std::unordered_map<const void *, int> cache;
+    static std::unordered_map<const void *, std::pair<size_t, int>> cache;
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(kernel);
-    if (it != cache.end()) return it->second;
+    if (it != cache.end() && it->second.first == smem) return it->second.second;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, GEMV_THREADS, 0) != cudaSuccess || n < 1) n = 1;
-    cache[kernel] = n;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, GEMV_THREADS, smem) != cudaSuccess || n < 1) n = 1;
+    cache[kernel] = {smem, n};
     return n;
 }
 
@@ -357,6 +466,18 @@ cudaError_t launch_gemv_q8_0(const int8_t *w_qs, const uint16_t *w_d, int64_t n_
     p.n_tasks = 0;
     p.batch = static_cast<int>(batch);
     const int nbl = (p.nb + 31) / 32;
+    if (batch >= 3 && epi != QG_EPI_SILU_MUL_HALVES && k % 256 == 0 && k <= 4096 &&
+        (reinterpret_cast<uintptr_t>(w_d) & 15) == 0) {
+        // tensor-core path: 16 rows per warp task, the batch's codes staged in shared memory
+        const void *kern = reinterpret_cast<const void *>(gemv_q8_0_mma_kernel);
+        const size_t smem = static_cast<size_t>(8) * (k + 32) + static_cast<size_t>(8) * (k / QK) * 4;
+        const int occ = max_ctas_per_sm(kern, smem);
+        const int wpc = GEMV_THREADS / 32;
+        const int64_t need = ((n_rows + MMA_ROWS - 1) / MMA_ROWS + wpc - 1) / wpc;
+        const int64_t cap = static_cast<int64_t>(num_sms()) * occ;
+        return launch_pdl(gemv_q8_0_mma_kernel, dim3(static_cast<unsigned>(need < cap ? need : cap)),
+                          dim3(GEMV_THREADS), smem, s, p);
+    }
     if (batch == 1) return dispatch_r<1>(p, nbl, s);
     if (batch == 2) return dispatch_r<2>(p, nbl, s);
     if (batch <= 4) return dispatch_r<4>(p, nbl, s);
