@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_q8_0_mma_kernel(const GemvP
     const int K = p.k, nb = p.nb;
     const int XS = K + 32;  // row stride of the staged codes: conflict-free 8-byte fragment loads
     int8_t *s_x = reinterpret_cast<int8_t *>(smem);
-    float *s_xd = reinterpret_cast<float *>(smem + 8 * XS);  // [8][nb]
+    float *s_xd = reinterpret_cast<float *>(smem + 8 * XS);  // [nb][8]: a thread's batch pair is one 8-byte load
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const int wpc = blockDim.x >> 5;
@@ -243,8 +243,8 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_q8_0_mma_kernel(const GemvP
         *reinterpret_cast<uint4 *>(s_x + b * XS + off) = v;
     }
     for (int i = threadIdx.x; i < 8 * nb; i += blockDim.x) {
-        const int b = i / nb;
-        s_xd[i] = b < p.batch ? h2f(p.xd[i]) : 0.0f;
+        const int b = i / nb, j = i - b * nb;
+        s_xd[j * 8 + b] = b < p.batch ? h2f(p.xd[i]) : 0.0f;
     }
     __syncthreads();
 
@@ -274,7 +274,8 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_q8_0_mma_kernel(const GemvP
                 const uint2 xf = *reinterpret_cast<const uint2 *>(s_x + g * XS + blk * QK + 8 * t);
                 int c[4] = {0, 0, 0, 0};
                 mma_s8_16832(c, a[u].x, b[u].x, a[u].y, b[u].y, xf.x, xf.y);
-                const float x0 = s_xd[(2 * t) * nb + blk], x1 = s_xd[(2 * t + 1) * nb + blk];
+                const float2 xs2 = *reinterpret_cast<const float2 *>(s_xd + blk * 8 + 2 * t);
+                const float x0 = xs2.x, x1 = xs2.y;
                 const float wa = h2f(sdA[u]), wb = h2f(sdB[u]);
                 acc[0] = fmaf(small_int_to_float(c[0]), wa * x0, acc[0]);
                 acc[1] = fmaf(small_int_to_float(c[1]), wa * x1, acc[1]);
