@@ -20,9 +20,10 @@
 // wait only on-chip work remains.  (Plain loads into registers would not do:
 // the compiler may legally sink read-only loads below the wait.)
 //
-// Shared-memory reads: lane j reads the 32-byte block j of a row as two 16-byte
-// halves, half (j >> 2) & 1 first, so every quarter-warp phase touches 32
-// distinct banks.  The activation words are paired in the same order.
+// Shared-memory reads are laid out so that every quarter-warp phase touches 32
+// distinct banks: in the GEMV kernels lane j reads the 32-byte block j of a row
+// as two 16-byte halves, half (j >> 2) & 1 first (activation words paired in the
+// same order); ffn_up_kernel stages its rows 16 bytes apart (see there).
 //
 //  * ffn_up_kernel: RMSNorm + Q8_0 quantization of x (every CTA, from L2),
 //    stacked gate|up block dots, SiLU(g)*u, and Q8_0 quantization of each
@@ -115,38 +116,42 @@ struct FfnUpParams {
 
 __host__ __device__ constexpr size_t ffn_up_smem_bytes(int k, bool down = false)
 {
-    // values [64][k] | scales [64][k/32] u16 | gamma [k] f32 | x codes [k] | x scales [k/32] f32
-    // | h [32] f32 | warp partial pairs [2 * 16] f32
+    // values [64][k + 16] | scales [64][k/32] u16 | gamma [k] f32 | row partials [warps][64] f32
+    // | warp partial pairs [2 * 16] f32
     // | (one-launch layer) down column block [k][32] int8 | its scales [k] u16 | this CTA's
     //   terms of every output [k] f32 | h codes [32] | h scale f32 (16 B)
-    return static_cast<size_t>(64) * k + 64 * (k / 32) * 2 + 4 * k + k + 4 * (k / 32) + 4 * 32 + 4 * 32 +
+    return static_cast<size_t>(64) * (k + 16) + 64 * (k / 32) * 2 + 4 * k +
+           static_cast<size_t>(2048) * ((k + 1023) / 1024) + 4 * 32 +
            (down ? static_cast<size_t>(32) * k + 2 * k + 4 * k + 32 + 16 : 0);
 }
 
 // One CTA per 32-output block of h (rows o..o+31 of gate and of up).
-// NBL = ceil(k / 1024) blocks per lane; warps = 8 * NBL, each owning 4 / NBL outputs.
-//
-// After the wait: thread t holds x[4t..4t+3]; the compensated sum of squares
-// is reduced per warp, the warp partials meet in shared memory (one barrier),
-// and every warp merges them with a shuffle tree and evaluates r itself.  Eight
-// threads quantize each 32-value block; the codes go through shared memory to
-// the lanes whose dot products read them (second barrier, which also covers
-// the staged weights).
+// NBL = ceil(k / 1024); 8 NBL warps.  Warp w = wl + 8 wh (wl < 8) owns the four
+// K blocks wl + 8 c + 32 wh (c < 4) of x and of all 64 stacked rows:
+//  * thread (w, l) holds x values 4 (l % 8) .. +3 of block wl + 8 (l / 8) + 32 wh,
+//    so the eight lanes of a block quantize it without leaving the warp, and the
+//    same eight lanes then dot that block against rows l % 8 + 8 i (i < 8), the
+//    block's codes passed around by shuffles;
+//  * staged rows are k + 16 bytes apart, so the eight lanes of a quarter-warp
+//    read eight different bank groups;
+//  * the four lane groups are summed first (lane offsets 16 and 8: block index
+//    bits 4 and 3), then the warps in shared memory (bits 2, 1, 0), which is the
+//    order of the streaming GEMV's butterfly over 32 lanes: for k <= 1024, h has
+//    the bits that rmsnorm_quantize -> qgemv_q8_0(SiLU) gives.
+// After the wait there are two CTA barriers: the norm statistic's (which also
+// checks the staged slab) and the row partials'; warp 0 then forms h = SiLU(g) u
+// and its Q8_0 block.
 template <int NBL, bool DOWN>
 __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
 {
-    constexpr int OPW = 4 / NBL;  // outputs per warp
-    constexpr int NV = 2 * OPW;   // row sums per warp (gate rows then up rows)
-    constexpr int NW = 8 * NBL;   // warps per CTA
+    constexpr int NW = 8 * NBL;  // warps per CTA
     extern __shared__ __align__(16) uint8_t smem[];
-    const int K = p.k, nb = p.nb;
+    const int K = p.k, nb = p.nb, KP = K + 16;
     int8_t *s_w = reinterpret_cast<int8_t *>(smem);
-    uint16_t *s_wd = reinterpret_cast<uint16_t *>(smem + 64 * K);
-    float *s_gamma = reinterpret_cast<float *>(smem + 64 * K + 128 * nb);
-    int8_t *s_xq = reinterpret_cast<int8_t *>(s_gamma + K);
-    float *s_xd = reinterpret_cast<float *>(s_xq + K);
-    float *s_h = s_xd + nb;
-    float *s_part = s_h + 32;
+    uint16_t *s_wd = reinterpret_cast<uint16_t *>(smem + 64 * KP);
+    float *s_gamma = reinterpret_cast<float *>(smem + 64 * KP + 128 * nb);
+    float *s_red = s_gamma + K;       // [NW][64]
+    float *s_part = s_red + NW * 64;  // [2 * NW]
     int8_t *s_dn = reinterpret_cast<int8_t *>(s_part + 32);        // [K][32] (DOWN)
     uint16_t *s_dnd = reinterpret_cast<uint16_t *>(s_dn + 32 * K);  // [K]     (DOWN)
     float *s_out = reinterpret_cast<float *>(s_dnd + K);            // [K]     (DOWN)
@@ -162,56 +167,59 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
     pdl_trigger();
 
     // ---- stage everything that does not depend on the previous kernel -------
-    // Bulk copies issued by one thread are serviced one after another, so the
-    // slab is cut into pieces (gamma, the two scale slabs, eight value slabs of
-    // eight rows) that lanes 0-10 of warp 0 issue in one instruction; all
-    // complete on s_bar.
-    if (t == 0) mbar_init(&s_bar, 1);
+    // Bulk copies issued by one thread are serviced one after another, so they
+    // are spread over lanes: warp 0 copies the 64 rows (two per lane), warp 1
+    // gamma, the two scale slabs and (one-launch layer) the down column block;
+    // all complete on s_bar.
+    if (t == 0) {
+        mbar_init(&s_bar, 1);
+        mbar_expect_tx(&s_bar, 4u * K + 128u * nb + 64u * K + (DOWN ? 34u * K : 0u));
+    }
     __syncthreads();
     if (warp == 0) {
-        constexpr int PR = 8;  // rows per value piece
-        const uint32_t sbytes = 64u * nb;
-        if (lane == 0) mbar_expect_tx(&s_bar, 4u * K + 2 * sbytes + 64u * K + (DOWN ? 34u * K : 0u));
-        __syncwarp();
-        if (DOWN && lane >= 3 + 64 / PR && lane < 3 + 64 / PR + 5) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int row = lane + 32 * h;  // stacked: gate rows, then up rows
+            const int64_t src = h == 0 ? ob + lane : p.half + ob + lane;
+            bulk_copy_g2s(s_w + row * KP, p.w_qs + src * K, static_cast<uint32_t>(K), &s_bar, l2_evict_first_policy());
+        }
+    } else if (warp == 1) {
+        if (DOWN && lane >= 3 && lane < 8) {
             // down column block b: four value pieces of K/4 rows x 32 bytes, then the K scales
-            const int v = lane - (3 + 64 / PR);
+            const int v = lane - 3;
             const int64_t cb = static_cast<int64_t>(blockIdx.x) * K;
             void *dst = v < 4 ? static_cast<void *>(s_dn + v * 8 * K) : static_cast<void *>(s_dnd);
             const void *src = v < 4 ? static_cast<const void *>(p.wdn_qs + (cb + v * (K / 4)) * QK)
                                     : static_cast<const void *>(p.wdn_d + cb);
             bulk_copy_g2s(dst, src, v < 4 ? 8u * K : 2u * K, &s_bar, l2_evict_first_policy());
         }
-        if (lane < 3 + 64 / PR) {
-            const int v = lane - 3;                      // value piece: rows PR v .. of the stacked 64
-            const int64_t vrow = (v < 32 / PR ? ob : p.half + ob - 32) + static_cast<int64_t>(PR) * v;
+        if (lane < 3) {
             const int64_t srow = lane == 1 ? ob : p.half + ob;
-            void *dst = lane == 0 ? static_cast<void *>(s_gamma)
-                      : lane < 3  ? static_cast<void *>(s_wd + (lane - 1) * 32 * nb)
-                                  : static_cast<void *>(s_w + PR * v * K);
-            const void *src = lane == 0 ? static_cast<const void *>(p.gamma)
-                            : lane < 3  ? static_cast<const void *>(p.w_d + srow * nb)
-                                        : static_cast<const void *>(p.w_qs + vrow * K);
-            const uint32_t bytes = lane == 0 ? 4u * K : lane < 3 ? sbytes : static_cast<uint32_t>(PR) * K;
-            const uint64_t pol = lane == 0 ? l2_evict_last_policy() : l2_evict_first_policy();
-            bulk_copy_g2s(dst, src, bytes, &s_bar, pol);
+            void *dst = lane == 0 ? static_cast<void *>(s_gamma) : static_cast<void *>(s_wd + (lane - 1) * 32 * nb);
+            const void *src = lane == 0 ? static_cast<const void *>(p.gamma) : static_cast<const void *>(p.w_d + srow * nb);
+            const uint32_t bytes = lane == 0 ? 4u * K : 64u * nb;
+            bulk_copy_g2s(dst, src, bytes, &s_bar, lane == 0 ? l2_evict_last_policy() : l2_evict_first_policy());
         }
     }
 
     pdl_wait();
 
-    // x first (the one input that comes from the previous kernel) ...
-    const bool live = 4 * t < K;
+    const int wl = warp & 7, wh = warp >> 3;
+    const int xb = wl + 8 * (lane >> 3) + 32 * wh;  // block of this thread's four x values (and of its dots)
+    const int xo = 32 * xb + 4 * (lane & 7);        // their offset in x
+    const bool live = xb < nb;
+    const int rg = lane & 7;                        // this lane's rows: rg + 8 i
+
     float4 xv4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (live) xv4 = *reinterpret_cast<const float4 *>(p.x + 4 * t);
+    if (live) xv4 = *reinterpret_cast<const float4 *>(p.x + xo);
     if constexpr (DOWN) {
-        // ... x = r + partials of the previous layer, all loads first, then the sum
+        // x = r + partials of the previous layer, all loads first, then the sum
         // in partial order (the order qg_decode_layer_finish uses)
         constexpr int MAXP = kMaxLayerPartials;
         float4 pv[MAXP];
 #pragma unroll
         for (int c = 0; c < MAXP; ++c)
-            if (c < p.n_in && live) pv[c] = *reinterpret_cast<const float4 *>(p.p_in + static_cast<int64_t>(c) * K + 4 * t);
+            if (c < p.n_in && live) pv[c] = *reinterpret_cast<const float4 *>(p.p_in + static_cast<int64_t>(c) * K + xo);
 #pragma unroll
         for (int c = 0; c < MAXP; ++c) {
             if (c < p.n_in && live) {
@@ -221,43 +229,7 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
                 xv4.w += pv[c].w;
             }
         }
-        if (blockIdx.x == 0 && live) *reinterpret_cast<float4 *>(p.r_next + 4 * t) = xv4;
-    }
-
-
-    // ... then the staged slab (long since arrived, normally).  A copy that has
-    // not landed within the limit leaves NaN outputs for this block.
-    const bool staged = __syncthreads_and(mbar_wait_bounded(&s_bar, 0, kCopyWaitLimitNs));
-    if (!staged) {
-        if (warp == 0) {
-            p.h[ob + lane] = __int_as_float(0x7fc00000);
-            p.hq[ob + lane] = 0;
-            if (lane == 0) p.hd[blockIdx.x] = 0x7e00;
-        }
-        mbar_wait_bounded(&s_bar, 0, kCopyWaitLimitNs);
-        // the one-launch layer still takes part in its cluster's reduction (NaN terms)
-        if constexpr (!DOWN) return;
-    }
-    const int c0 = lane_half(lane);
-    if (staged) {
-    // While x is in flight, pull this warp's weight rows out of shared memory
-    // into registers (rows: OPW gate rows, then OPW up rows).
-    u32x8 wr[NV][NBL];
-    float wsc[NV][NBL];
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-        const int row = (i < OPW) ? warp * OPW + i : 32 + warp * OPW + (i - OPW);
-#pragma unroll
-        for (int j = 0; j < NBL; ++j) {
-            const int blk = lane + 32 * j;
-            if (blk < nb) {
-                wr[i][j] = ld_block_halves(s_w + row * K + blk * QK, c0);
-                wsc[i][j] = h2f(s_wd[row * nb + blk]);
-            } else {
-                zero(wr[i][j]);
-                wsc[i][j] = 0.0f;
-            }
-        }
+        if (blockIdx.x == 0 && live) *reinterpret_cast<float4 *>(p.r_next + xo) = xv4;
     }
 
     // ---- RMSNorm statistic ---------------------------------------------------
@@ -273,9 +245,25 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
         s_part[2 * warp] = acc.hi;
         s_part[2 * warp + 1] = acc.lo;
     }
-    __syncthreads();
+    // The same barrier publishes the staged slab (thread 0 has seen it land,
+    // normally long ago).  A copy that has not landed within the limit leaves
+    // NaN outputs for this block.
+    const bool staged = __syncthreads_and(t != 0 || mbar_wait_bounded(&s_bar, 0, kCopyWaitLimitNs));
+    if (!staged) {
+        if (warp == 0) {
+            p.h[ob + lane] = __int_as_float(0x7fc00000);
+            p.hq[ob + lane] = 0;
+            if (lane == 0) p.hd[blockIdx.x] = 0x7e00;
+        }
+        mbar_wait_bounded(&s_bar, 0, kCopyWaitLimitNs);
+        // the one-launch layer still takes part in its cluster's reduction (NaN terms)
+        if constexpr (!DOWN) return;
+    }
+    if (staged) {
     f32pair tot = {0.0f, 0.0f};
     if (lane < NW) tot = f32pair{s_part[2 * lane], s_part[2 * lane + 1]};
+    float4 g4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (live) g4 = *reinterpret_cast<const float4 *>(s_gamma + xo);
 #pragma unroll
     for (int off = NW / 2; off >= 1; off >>= 1) {
         f32pair o;
@@ -288,15 +276,15 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
     const float r = rms_inv_from_pair(tot, K, p.inv_k, p.eps);
 
     // ---- Q8_0 quantization of x_hat = (x * r) * gamma, eight threads per block
+    uint32_t xc = 0u;  // this thread's four codes
+    float xdf = 0.0f;  // its block's scale (binary16 value)
     {
-        const int b = t >> 3, sub = t & 7;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (live) {
-            const float4 g = *reinterpret_cast<const float4 *>(s_gamma + 4 * t);
-            v.x = __fmul_rn(__fmul_rn(xv4.x, r), g.x);
-            v.y = __fmul_rn(__fmul_rn(xv4.y, r), g.y);
-            v.z = __fmul_rn(__fmul_rn(xv4.z, r), g.z);
-            v.w = __fmul_rn(__fmul_rn(xv4.w, r), g.w);
+            v.x = __fmul_rn(__fmul_rn(xv4.x, r), g4.x);
+            v.y = __fmul_rn(__fmul_rn(xv4.y, r), g4.y);
+            v.z = __fmul_rn(__fmul_rn(xv4.z, r), g4.z);
+            v.w = __fmul_rn(__fmul_rn(xv4.w, r), g4.w);
         }
         float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
@@ -304,58 +292,70 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
         if (live) {
             const float dd = div127(m);
-            const uint32_t c = q8_pack4(v, dd, __frcp_rn(dd));
-            reinterpret_cast<uint32_t *>(s_xq)[t] = c;
+            xc = q8_pack4(v, dd, __frcp_rn(dd));
             const uint16_t dbits = f2h_rn(dd);
-            if (sub == 0) s_xd[b] = h2f(dbits);
+            xdf = h2f(dbits);
             if (blockIdx.x == 0) {
-                if (p.xq_out) reinterpret_cast<uint32_t *>(p.xq_out)[t] = c;
-                if (p.xd_out && sub == 0) p.xd_out[b] = dbits;
+                if (p.xq_out) reinterpret_cast<uint32_t *>(p.xq_out)[xo / 4] = xc;
+                if (p.xd_out && (lane & 7) == 0) p.xd_out[xb] = dbits;
             }
         }
         if (blockIdx.x == 0 && t == 0 && p.r_out) *p.r_out = r;
     }
-    __syncthreads();
 
-    u32x8 xv[NBL];
-    float xs[NBL];
+    // ---- block dots: block xb of rows rg + 8 i ---------------------------------
+    // word s of the block is held by lane 8 (lane / 8) + s
+    u32x8 xw;
+    const int src = lane & 24;
 #pragma unroll
-    for (int j = 0; j < NBL; ++j) {
-        const int blk = lane + 32 * j;
-        if (blk < nb) {
-            xv[j] = ld_block_halves(s_xq + blk * QK, c0);
-            xs[j] = s_xd[blk];
-        } else {
-            zero(xv[j]);
-            xs[j] = 0.0f;
+    for (int s = 0; s < 8; ++s) xw.v[s] = __shfl_sync(0xffffffffu, xc, src + s);
+    const float xs = __shfl_sync(0xffffffffu, xdf, src);
+    float part[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int row = rg + 8 * i;
+        part[i] = live ? block_term(ld_block_halves(s_w + row * KP + xb * QK, 0), xw, h2f(s_wd[row * nb + xb]), xs, 0.0f)
+                       : 0.0f;
+    }
+    // the four lane groups of a row: offset 16 (block bit 4), then 8 (bit 3); a
+    // lane keeps half of its values each time and ends with rows rg + 8 (2 (lane / 8) + k)
+    float v4[4], v2[2];
+    {
+        const bool up = (lane & 16) != 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float send = up ? part[k] : part[k + 4];
+            const float keep = up ? part[k + 4] : part[k];
+            v4[k] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
         }
     }
-
-    // ---- block dots: OPW gate rows and OPW up rows ----------------------------
-    float part[NV];
+    {
+        const bool up = (lane & 8) != 0;
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-        float a = 0.0f;
+        for (int k = 0; k < 2; ++k) {
+            const float send = up ? v4[k] : v4[k + 2];
+            const float keep = up ? v4[k + 2] : v4[k];
+            v2[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+    }
 #pragma unroll
-        for (int j = 0; j < NBL; ++j) a = block_term(wr[i][j], xv[j], wsc[i][j], xs[j], a);
-        part[i] = a;
-    }
-    const float tot_row = warp_sum_many<NV>(part, lane);
-    // lane holds value index (lane & 16 ? NV/2 : 0) + ...: the gate of output i
-    // sits in a lane with bit 4 clear, its up value in the lane with bit 4 set.
-    const float up = __shfl_xor_sync(0xffffffffu, tot_row, 16);
-    constexpr int REP = 32 / NV;  // lanes holding the same value
-    if ((lane & 16) == 0 && (lane & (REP - 1)) == 0) {
-        const int i = (lane & 15) / REP;  // output within the warp
-        const float hv = silu_mul(tot_row, up);
-        s_h[warp * OPW + i] = hv;
-        p.h[ob + warp * OPW + i] = hv;
-    }
+    for (int k = 0; k < 2; ++k) s_red[warp * 64 + rg + 8 * (2 * (lane >> 3) + k)] = v2[k];
     __syncthreads();
 
-    // ---- Q8_0 quantization of this CTA's 32-value block of h -----------------
+    // ---- warp 0: row totals over the warps (block bits 2, 1, 0: warp offsets 4,
+    // 2, 1), SiLU(g) u, and the Q8_0 block of h ----------------------------------
     if (warp == 0) {
-        const float v = s_h[lane];
+        auto row_total = [&](int row) {
+            const float *c = s_red + row;
+            float s = ((c[0] + c[4 * 64]) + (c[2 * 64] + c[6 * 64])) + ((c[64] + c[5 * 64]) + (c[3 * 64] + c[7 * 64]));
+            if constexpr (NBL == 2) {
+                c += 8 * 64;
+                s += ((c[0] + c[4 * 64]) + (c[2 * 64] + c[6 * 64])) + ((c[64] + c[5 * 64]) + (c[3 * 64] + c[7 * 64]));
+            }
+            return s;
+        };
+        const float v = silu_mul(row_total(lane), row_total(32 + lane));
+        p.h[ob + lane] = v;
         const float m = warp_max(fabsf(v));
         const float dd = div127(m);
         const int8_t code = static_cast<int8_t>(q8_code(v, dd, __frcp_rn(dd)));
@@ -373,6 +373,7 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
         __syncthreads();  // h codes
         constexpr int RPW_MAX = 128;  // rows per warp: K / (8 NBL) <= 128
         const int rpw = K / NW;
+        const int c0 = lane_half(lane);
         const u32x8 hv = ld_block_halves(s_hq, c0);
         const float dh = *s_hd;
 #pragma unroll

@@ -182,20 +182,6 @@ __device__ __forceinline__ void s8x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t
     hi = *reinterpret_cast<const uint32_t *>(&rb);
 }
 
-// try_wait with a suspend-time hint: a thread whose phase is not complete
-// sleeps in the barrier unit (waking when the phase completes, or after
-// hint_ns) instead of spinning and taking issue slots from the working warps.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
-{
-    uint32_t ok;
-    asm volatile(
-        "{ .reg .pred q; mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2, %3; selp.u32 %0, 1, 0, q; }"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
-}
-
 // Bounded wait on phase `parity`; gives up when another role has aborted.
 __device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
 {
