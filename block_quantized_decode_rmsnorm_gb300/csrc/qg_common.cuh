@@ -82,6 +82,17 @@ __device__ __forceinline__ u32x8 ld_stream_32B(const void *p, uint64_t pol)
 
 __device__ __forceinline__ void prefetch_l2(const void *p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
+// 16 bytes of streamed, read-only data (weights): not kept in L1, with a
+// 256-byte L2 prefetch hint.  p must be 16-byte aligned.
+__device__ __forceinline__ uint4 ld_stream_16B(const void *p)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
 // 16 bytes through the read-only path.  p must be 16-byte aligned.
 __device__ __forceinline__ uint4 ld_nc_16B(const void *p)
 {

@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(BF16_THREADS) gemv_bf16_kernel(const Bf16Param
         {                                                                                        \
             const int g = lane + 32 * ((C0) + c);                                                \
             if (row >= 0 && g < p.n_groups)                                                      \
-                w[s][c] = ld_nc_16B(p.w + row * p.k + g * 8);                                    \
+                w[s][c] = ld_stream_16B(p.w + row * p.k + g * 8);                                \
             else                                                                                 \
                 w[s][c] = make_uint4(0u, 0u, 0u, 0u);                                            \
         }                                                                                        \
