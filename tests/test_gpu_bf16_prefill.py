@@ -58,6 +58,26 @@ def test_bf16_gemv(torch, orc, n, k, norm, epi):
         assert_close(y, y64, a64, TOL_BF16, "bf16")
 
 
+def test_bf16_gemv_weights_16_byte_aligned(torch, orc):
+    """Weights starting 16 bytes past a 32-byte boundary (the smallest alignment
+    the boundary accepts): same tolerance."""
+    from block_quantized_decode_rmsnorm_gb300 import api
+
+    n, k = 96, 1024
+    case = synth.bf16_case(5, n_rows=n, k=k)
+    big = torch.empty((n * k + 8,), dtype=torch.bfloat16, device="cuda")
+    w = big[8:].view(n, k)
+    assert w.data_ptr() % 32 == 16
+    w.copy_(_bf16(case["w"], torch))
+    y = api.qgemv_bf16(w, _bf16(case["x"], torch), _bf16(case["gamma"], torch), EPS, epilogue="silu_mul")
+    torch.cuda.synchronize()
+    y64, a64, _, _ = orc.gemv_bf16(case["w"], case["x"], case["gamma"], EPS)
+    F = n // 2
+    g, u = y64[:F], y64[F:]
+    assert_close(y.cpu().numpy(), orc.silu_mul(g, u), silu_scale(g, u, a64[:F], a64[F:], TOL_BF16), TOL_BF16,
+                 "bf16 silu, 16-byte aligned rows")
+
+
 def test_bf16_matches_q8_bound_when_exact(torch, orc):
     """With the norm off the f32 accumulation error is far inside the bf16 bar;
     check the much tighter Q8_0 bar too, so that a lost term cannot hide in 2e-3."""
