@@ -169,6 +169,18 @@ __device__ __forceinline__ float warp_sum_many(float (&v)[NV], int lane)
     return v[0];
 }
 
+// max |v| over the warp with fmaxf's treatment of NaN (ignored unless every lane
+// holds one), in two warp reductions instead of five shuffles: the bit patterns
+// of non-negative floats order as unsigned integers.
+__device__ __forceinline__ float warp_max_abs(float v)
+{
+    const float a = fabsf(v);
+    const bool nan = a != a;
+    const uint32_t m = __reduce_max_sync(0xffffffffu, nan ? 0u : __float_as_uint(a));
+    const uint32_t all_nan = __reduce_and_sync(0xffffffffu, nan ? 1u : 0u);
+    return all_nan ? __uint_as_float(0x7fffffffu) : __uint_as_float(m);
+}
+
 __device__ __forceinline__ float warp_max(float v)
 {
 #pragma unroll

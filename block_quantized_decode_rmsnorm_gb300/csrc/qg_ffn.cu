@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
         };
         const float v = silu_mul(row_total(lane), row_total(32 + lane));
         p.h[ob + lane] = v;
-        const float m = warp_max(fabsf(v));
+        const float m = warp_max_abs(v);
         const float dd = div127(m);
         const int8_t code = static_cast<int8_t>(q8_code(v, dd, __frcp_rn(dd)));
         const uint16_t dbits = f2h_rn(dd);
@@ -482,7 +482,11 @@ __global__ void __launch_bounds__(256) gemv_prefetch_kernel(const PrefetchParams
     // lane l of warp w holds the residual of row w + l * nw (rows of this CTA)
     float res = 0.0f;
     if (p.epi == QG_EPI_RESIDUAL_ADD && warp + lane * nw < nrow) res = p.residual[r0 + warp + lane * nw];
-    if (!__syncthreads_and(mbar_wait_bounded(&s_bar, 0, kCopyWaitLimitNs))) {
+    // Every thread sees the staged slab land itself (normally long ago), so the
+    // weight reads below overlap the activation's L2 round trip; a warp owns its
+    // rows (and their residuals), so no CTA barrier is needed.  A copy that has
+    // not landed within the limit leaves NaN outputs for this warp's rows.
+    if (!mbar_wait_bounded(&s_bar, 0, kCopyWaitLimitNs)) {
         for (int rr = warp; rr < nrow; rr += nw)
             if (lane == 0) p.y[r0 + rr] = __int_as_float(0x7fc00000);
         mbar_wait_bounded(&s_bar, 0, kCopyWaitLimitNs);
