@@ -225,6 +225,40 @@ def time_graph(torch, g, iters: int) -> float:
     return e0.elapsed_time(e1) / 1e3 / iters
 
 
+def replay_trials(torch, g, per: int, trials: int = 20) -> dict:
+    """Seconds per launch over `trials` separately timed replays of g (each
+    replay `per` launches): median, 10th and 90th percentiles."""
+    g.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(trials):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) / 1e3 / per)
+    ts.sort()
+    return {"median": statistics.median(ts), "p10": ts[round(0.1 * (trials - 1))],
+            "p90": ts[round(0.9 * (trials - 1))], "trials": trials}
+
+
+def cold_and_warm(torch, launch, ws, wbytes: int) -> dict:
+    """Per-launch time of launch(w): cold, over the rotating copies ws (>= 4x L2,
+    one graph), and warm, 20 launches on ws[0] (only where a copy fits in half
+    of L2), each over 20 timed replays."""
+    g = capture(torch, lambda: [launch(w) for w in ws])
+    st = replay_trials(torch, g, len(ws))
+    del g
+    out = {"us": st["median"] * 1e6, "us_p10": st["p10"] * 1e6, "us_p90": st["p90"] * 1e6,
+           "trials": st["trials"], "copies": len(ws)}
+    if 2 * wbytes <= torch.cuda.get_device_properties(0).L2_cache_size:
+        gw = capture(torch, lambda: [launch(ws[0]) for _ in range(20)])
+        out["us_warm_l2"] = replay_trials(torch, gw, 20)["median"] * 1e6
+        del gw
+    return out
+
+
 def l2_copies(torch, bytes_one: int) -> int:
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     return max(2, -(-4 * l2 // bytes_one))
@@ -240,7 +274,9 @@ def replicate_q8(torch, api, w0, copies: int):
 
 
 def extra_configs(torch, pk) -> dict:
-    """Kernel rates on the other workloads, each cold (rotating copies >= 4x L2)."""
+    """Kernel rates on the other workloads: cold (rotating copies >= 4x L2; median,
+    p10 and p90 of 20 timed replays) and, where the weights fit in L2, warm
+    (`us_warm_l2`, labelled as such)."""
     import numpy as np
 
     from block_quantized_decode_rmsnorm_gb300 import api, synth
@@ -257,12 +293,11 @@ def extra_configs(torch, pk) -> dict:
         x = torch.from_numpy(synth.f32_normal(0, synth.S_X, (batch, k))).cuda()
         xq, xd = api.quantize_act_q8_0(x)
         y = torch.empty((batch, n), dtype=torch.float32, device="cuda")
-        g = capture(torch, lambda: [api.qgemv_q8_0(w, xq, xd, y=y) for w in ws])
-        t = time_graph(torch, g, 5) / copies
+        r = cold_and_warm(torch, lambda w: api.qgemv_q8_0(w, xq, xd, y=y), ws, wbytes)
         algo = wbytes + batch * (k + (k // 32) * 2) + batch * n * 4
-        gbs = algo / t / 1e9
-        out[name] = {"us": t * 1e6, "GB/s": gbs, "frac_hbm": gbs / hbm, "bytes": algo, "copies": copies}
-        del ws, g
+        gbs = algo / (r["us"] / 1e6) / 1e9
+        out[name] = {**r, "GB/s": gbs, "frac_hbm": gbs / hbm, "bytes": algo}
+        del ws
 
     gemv_rate("q8_0_gemv_256x1024_b1", 256, 1024, 1)
     for b in (1, 2, 4, 8):
@@ -275,12 +310,12 @@ def extra_configs(torch, pk) -> dict:
     ws = [w0] + [w0.clone() for _ in range(copies - 1)]
     xb, gb = api.bf16_from_bits(bc["x"]), api.bf16_from_bits(bc["gamma"])
     yb = torch.empty((w0.shape[0] // 2,), dtype=torch.float32, device="cuda")
-    g = capture(torch, lambda: [api.qgemv_bf16(w, xb, gb, EPS, epilogue="silu_mul", y=yb) for w in ws])
-    t = time_graph(torch, g, 5) / copies
+    r = cold_and_warm(torch, lambda w: api.qgemv_bf16(w, xb, gb, EPS, epilogue="silu_mul", y=yb), ws,
+                      w0.numel() * 2)
     algo = w0.numel() * 2 + 2 * 2 * w0.shape[1] + yb.numel() * 4
-    out["bf16_proj_18432x2560_norm_silu"] = {"us": t * 1e6, "GB/s": algo / t / 1e9,
-                                             "frac_hbm": algo / t / 1e9 / hbm, "bytes": algo, "copies": copies}
-    del ws, g
+    gbs = algo / (r["us"] / 1e6) / 1e9
+    out["bf16_proj_18432x2560_norm_silu"] = {**r, "GB/s": gbs, "frac_hbm": gbs / hbm, "bytes": algo}
+    del ws
 
     # prompt-sized contraction: tensor-core path (activation tiles, tcgen05) at
     # the library's tile width and at each fixed one, and the int8 mma.sync
@@ -300,12 +335,9 @@ def extra_configs(torch, pk) -> dict:
                          lambda w, bn=bn: api.qgemm_q8_0_prefill_tc(w, xt, y=yp, tile_n=bn)))
     variants.append(("prefill_512x7168x1024_mma_sync", lambda w: api.qgemm_q8_0_prefill(w, xq, xd, y=yp)))
     for name, fn in variants:
-        g = capture(torch, lambda: [fn(w) for w in wps])
-        t = time_graph(torch, g, 5) / copies
-        tops = ops / t / 1e12
-        out[name] = {"us": t * 1e6, "TOPS": tops, "frac_f16_dense_peak": tops / pk["bf16_tflops"], "int_ops": ops,
-                     "copies": copies}
-        del g
+        r = cold_and_warm(torch, fn, wps, wp.nbytes)
+        tops = ops / (r["us"] / 1e6) / 1e12
+        out[name] = {**r, "TOPS": tops, "frac_f16_dense_peak": tops / pk["bf16_tflops"], "int_ops": ops}
     del wps
     torch.cuda.empty_cache()
     _ = np
