@@ -315,7 +315,21 @@ def extra_configs(torch, pk) -> dict:
     algo = w0.numel() * 2 + 2 * 2 * w0.shape[1] + yb.numel() * 4
     gbs = algo / (r["us"] / 1e6) / 1e9
     out["bf16_proj_18432x2560_norm_silu"] = {**r, "GB/s": gbs, "frac_hbm": gbs / hbm, "bytes": algo}
-    del ws
+
+    # bf16 gate|up for a 512-row prompt on tcgen05: the whole call (row norms, then
+    # the projection with SiLU*u), and the projection alone on normalised rows
+    xp = api.bf16_from_bits(synth.bf16_normal_bits(0, synth.S_X + 7, (512, w0.shape[1])))
+    xh = torch.empty_like(xp)
+    yp16 = torch.empty((512, w0.shape[0] // 2), dtype=torch.float32, device="cuda")
+    flops = 2 * 512 * w0.shape[0] * w0.shape[1]
+    for name, fn in (("prefill_bf16_512x18432x2560_norm_silu",
+                      lambda w: api.qgemm_bf16_prefill(w, xp, gb, EPS, epilogue="silu_mul", y=yp16, xhat=xh)),
+                     ("prefill_bf16_512x18432x2560_silu_gemm_only",
+                      lambda w: api.qgemm_bf16_prefill(w, xh, None, EPS, epilogue="silu_mul", y=yp16))):
+        r = cold_and_warm(torch, fn, ws, w0.numel() * 2)
+        tf = flops / (r["us"] / 1e6) / 1e12
+        out[name] = {**r, "TFLOP/s": tf, "frac_bf16_dense_peak": tf / pk["bf16_tflops"], "flops": flops}
+    del ws, xp, xh, yp16
 
     # prompt-sized contraction: tensor-core path (activation tiles, tcgen05) at
     # the library's tile width and at each fixed one, and the int8 mma.sync
@@ -559,6 +573,14 @@ def run_workload(args):
         y = torch.empty((b, 262144), dtype=torch.float32, device="cuda")
         fn = lambda: api.qgemv_q8_0(wt, xq, xd, y=y)
         name = f"output head 262144x1024, batch {b}"
+    elif w == "prefill_bf16":
+        bc = synth.bf16_case(0)
+        wb, gb = api.bf16_from_bits(bc["w"]), api.bf16_from_bits(bc["gamma"])
+        xb = api.bf16_from_bits(synth.bf16_normal_bits(0, synth.S_X + 7, (512, bc["w"].shape[1])))
+        xh = torch.empty_like(xb)
+        y = torch.empty((512, bc["w"].shape[0] // 2), dtype=torch.float32, device="cuda")
+        fn = lambda: api.qgemm_bf16_prefill(wb, xb, gb, EPS, epilogue="silu_mul", y=y, xhat=xh)
+        name = "bf16 gate|up 18432x2560 + RMSNorm + SiLU*u, 512-row prompt, tcgen05"
     else:  # bf16
         bc = synth.bf16_case(0)
         wb, xb, gb = api.bf16_from_bits(bc["w"]), api.bf16_from_bits(bc["x"]), api.bf16_from_bits(bc["gamma"])
@@ -636,7 +658,7 @@ def main():
     ap.add_argument("--path", choices=["one", "two", "four"], default="two",
                     help="launches per decode layer: one (split-K down inside the layer kernel), two, four")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--workload", choices=["prefill", "head1", "head2", "head4", "head8", "bf16"],
+    ap.add_argument("--workload", choices=["prefill", "prefill_bf16", "head1", "head2", "head4", "head8", "bf16"],
                     help="time one workload's kernel alone (for profiling) instead of the bench step")
     args = ap.parse_args()
     if args.warmup < 3:

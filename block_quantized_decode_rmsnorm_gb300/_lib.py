@@ -36,6 +36,7 @@ SIGNATURES = {
     "qgemv_bf16": (ST, [P, I64, I64, P, P, F32, I32, P, P, P]),
     "qgemm_q8_0_prefill": (ST, [P, P, I64, I64, P, P, I64, P, P]),
     "qgemm_q8_0_prefill_tc": (ST, [P, P, I64, I64, P, I64, P, I32, P]),
+    "qgemm_bf16_prefill": (ST, [P, I64, I64, P, I64, P, F32, I32, P, P, P]),
     "qg_ffn_up_q8_0": (ST, [P, P, I64, F32, P, P, I64, P, P, P, P, P, P, P]),
     "qg_decode_ffn_q8_0": (ST, [P, P, I64, I64, F32, P, P, P, P, P, P, P, P]),
     "qg_decode_layer_q8_0": (ST, [P, P, I32, P, P, P, I64, I64, F32, P, P, P, P, P, P, P, P]),

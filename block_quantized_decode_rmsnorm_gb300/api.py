@@ -206,6 +206,33 @@ def qgemv_bf16(w: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor | None = No
     return y
 
 
+def qgemm_bf16_prefill(w: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor | None = None, eps: float = 1e-6,
+                       epilogue: str | int = "none", y: torch.Tensor | None = None,
+                       xhat: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """qgemv_bf16 for m prompt rows at once on the tensor cores: x bf16 [m, k],
+    w bf16 [n, k]; y f32 [m, n_out].  xhat (bf16 [m, k]) is the work buffer of
+    the normalised rows, allocated here when not given and gamma is."""
+    epi = EPILOGUES[epilogue] if isinstance(epilogue, str) else int(epilogue)
+    _need(w, "w", torch.bfloat16)
+    n_rows, k = w.shape
+    if x.dim() != 2 or x.shape[1] != k:
+        raise ValueError(f"x: expected [m, {k}], got {tuple(x.shape)}")
+    _need(x, "x", torch.bfloat16, tuple(x.shape))
+    m = x.shape[0]
+    if gamma is not None:
+        _need(gamma, "gamma", torch.bfloat16, (k,))
+        if xhat is None:
+            xhat = torch.empty((m, k), dtype=torch.bfloat16, device=w.device)
+        _need(xhat, "xhat", torch.bfloat16, (m, k))
+    n_out = n_rows // 2 if epi == QG_EPI_SILU_MUL_HALVES else n_rows
+    if y is None:
+        y = torch.empty((m, n_out), dtype=torch.float32, device=w.device)
+    _need(y, "y", torch.float32, (m, n_out))
+    _lib.call("qgemm_bf16_prefill", w.data_ptr(), n_rows, k, x.data_ptr(), m, _ptr(gamma), float(eps), epi,
+              _ptr(xhat), y.data_ptr(), _stream_handle(stream))
+    return y
+
+
 def qgemm_q8_0_prefill(w: Q8Weight, xq: torch.Tensor, xd: torch.Tensor, y: torch.Tensor | None = None,
                        stream=None) -> torch.Tensor:
     """Prompt-sized block-scaled contraction; Y f32 [m, n_rows]."""

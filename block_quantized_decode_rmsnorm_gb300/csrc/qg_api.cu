@@ -37,6 +37,9 @@ cudaError_t launch_decode_layers_noalloc(const float *, float *, int, const floa
                                          int64_t, int64_t, float, cudaStream_t);
 cudaError_t launch_quantize_act_tiles(const float *, int64_t, int64_t, void *, cudaStream_t);
 bool prefill_tc_supported(int64_t k);
+bool prefill_bf16_supported(int64_t k);
+cudaError_t launch_prefill_bf16(const uint16_t *, int64_t, int64_t, const uint16_t *, int64_t, const uint16_t *, float,
+                                int, uint16_t *, float *, cudaStream_t);
 cudaError_t launch_prefill_tc(const int8_t *, const uint16_t *, int64_t, int64_t, const void *, int64_t, float *, int,
                               cudaStream_t);
 cudaError_t launch_gemv_prefetch(const int8_t *, const uint16_t *, int64_t, int64_t, const int8_t *, const uint16_t *,
@@ -351,6 +354,24 @@ qg_status qgemm_q8_0_prefill_tc(const int8_t *w_qs, const uint16_t *w_d, int64_t
     if (!w_qs || !w_d || !xt || !y) return QG_ERR_NULL;
     if (!aligned(w_qs, 32) || !aligned(w_d, 16) || !aligned(xt, 16) || !aligned(y, 16)) return QG_ERR_ALIGN;
     return from_cuda(qg::launch_prefill_tc(w_qs, w_d, n_rows, k, xt, m, y, tile_n, stream));
+}
+
+qg_status qgemm_bf16_prefill(const uint16_t *w, int64_t n_rows, int64_t k, const uint16_t *x, int64_t m,
+                             const uint16_t *gamma, float eps, int epilogue, uint16_t *xhat, float *y,
+                             qg_stream_t stream)
+{
+    if (n_rows < 0 || n_rows > kMaxRows || n_rows > INT32_MAX) return QG_ERR_SHAPE;
+    if (m < 0 || m > (int64_t(1) << 24)) return QG_ERR_SHAPE;
+    if (k <= 0 || k > 16384 || !qg::prefill_bf16_supported(k)) return QG_ERR_SHAPE;
+    if (!(eps >= 0.0f)) return QG_ERR_SHAPE;
+    if (epilogue != QG_EPI_NONE && epilogue != QG_EPI_SILU_MUL_HALVES) return QG_ERR_UNSUPPORTED;
+    if (epilogue == QG_EPI_SILU_MUL_HALVES && (n_rows % 2) != 0) return QG_ERR_SHAPE;
+    if (n_rows == 0 || m == 0) return QG_OK;
+    if (!w || !x || !y || (gamma && !xhat)) return QG_ERR_NULL;
+    if (!aligned(w, 16) || !aligned(x, 16) || !aligned(gamma, 16) || !aligned(xhat, 16) || !aligned(y, 16))
+        return QG_ERR_ALIGN;
+    if (gamma && overlap(x, xhat, static_cast<size_t>(m) * k * 2)) return QG_ERR_SHAPE;
+    return from_cuda(qg::launch_prefill_bf16(w, n_rows, k, x, m, gamma, eps, epilogue, xhat, y, stream));
 }
 
 qg_status qg_debug_block_dots_q8_0(const int8_t *w_qs, int64_t n_rows, int64_t k, const int8_t *xq, int64_t batch,

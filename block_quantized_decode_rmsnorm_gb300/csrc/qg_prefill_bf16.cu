@@ -1,0 +1,302 @@
+// bf16 prompt-sized projection on tcgen05: Y = x_hat W^T for M prompt rows, with
+// the RMSNorm in front (x_hat = bf16((x * r) * gamma) per row) and SiLU(g) * u or
+// nothing behind.  The decode form of the same operation is qgemv_bf16.
+//
+// "One level down: #002 the same compiler on a GPU": The numerical contract
+// (bf16 weights and activations, f32 accumulators); Emitting for a GPU (the
+// normalization fused with the projection that follows it, the activation with
+// the projection before it; the stacked gate|up projection).  "Filling in the
+// blanks: Inference using Phobos", Fast Decode (a prompt reuses every weight
+// for all of its rows, so that form belongs on the tensor cores).
+//
+// GB300 mapping.  One small kernel writes x_hat for all M rows (one CTA per row,
+// the same compensated norm statistic as the GEMV).  The projection is a
+// persistent warp-specialised kernel over 128 x 256 output tiles:
+//  * one thread issues TMA copies (128-byte swizzle) of a 128 x 64 x_hat slab and
+//    two 128 x 64 weight slabs per K step into a four-stage ring; for SiLU(g) * u
+//    the two weight slabs are the gate rows and the matching up rows, so one MMA
+//    of N = 256 produces both halves of 128 outputs;
+//  * one thread issues four tcgen05.mma kind::f16 (bf16 A and B, M = 128,
+//    N = 256, K = 16) per stage into a TMEM accumulator (two of 256 columns, so
+//    the epilogue of one tile overlaps the main loop of the next);
+//  * four epilogue warps read the accumulator with tcgen05.ld and store f32
+//    outputs (SiLU(g) * u from the two halves where asked).
+// Products of bf16 values are exact in f32 and the MMA accumulates in f32, as
+// the numerical contract asks; only the summation order differs from a GEMV.
+// Every barrier wait is bounded by the global timer; a stalled pipeline aborts
+// (NaN outputs for the tiles left) instead of hanging.
+#include <cuda.h>
+#include <mutex>
+
+#include "qg_common.cuh"
+#include "qg_norm.cuh"
+#include "qg_tc.cuh"
+
+namespace qg {
+
+constexpr int PB_BM = 128;      // prompt rows per tile (TMEM lanes)
+constexpr int PB_BN = 256;      // accumulator columns per tile (MMA N)
+constexpr int PB_BK = 64;       // K per stage: one 128-byte swizzle row of bf16
+constexpr int PB_STAGES = 4;
+constexpr int PB_A_BYTES = PB_BM * PB_BK * 2;        // 16 KB
+constexpr int PB_B_BYTES = PB_BN * PB_BK * 2;        // 32 KB
+constexpr int PB_STAGE = PB_A_BYTES + PB_B_BYTES;    // 48 KB, a multiple of 1024
+constexpr int PB_SMEM = PB_STAGES * PB_STAGE + 1024; // + alignment of the base
+constexpr int PB_EPI_WARPS = 4;
+constexpr int PB_TMA_WARP = 4;
+constexpr int PB_MMA_WARP = 5;
+constexpr int PB_THREADS = 6 * 32;
+
+struct PrefillBf16Params {
+    float *y;         // [m][n_out]
+    int64_t m;
+    int64_t n_out;    // outputs per row: half (SiLU * u) or n_rows
+    int64_t half;     // SiLU * u: up rows start here
+    int k;
+    int silu;         // 1: outputs are SiLU(g) * u of the stacked halves
+    int64_t m_tiles;
+    int64_t tiles;    // m_tiles * n_tiles, M fastest
+    int n_per_tile;   // outputs per tile: 128 (SiLU * u) or 256
+};
+
+// ---------------------------------------------------------------------------
+// x_hat for every prompt row
+// ---------------------------------------------------------------------------
+// One CTA per row: r from the compensated sum of exact squares (as in the GEMV),
+// then x_hat = bf16((x * r) * gamma), two f32 roundings and one bf16 rounding.
+__global__ void __launch_bounds__(256) rmsnorm_bf16_rows_kernel(const uint16_t *x, const uint16_t *gamma, int k,
+                                                                float inv_k, float eps, uint16_t *xhat)
+{
+    __shared__ float scratch[2 * 8 + 1];
+    const int64_t row = blockIdx.x;
+    const uint16_t *xr = x + row * k;
+    pdl_trigger();
+    pdl_wait();
+    f32pair acc = {0.0f, 0.0f};
+    for (int i = threadIdx.x; i < k; i += blockDim.x) pair_add_square(acc, __uint_as_float(static_cast<uint32_t>(xr[i]) << 16));
+    const float r = block_rms_inv(acc, k, inv_k, eps, scratch);
+    for (int i = threadIdx.x; i < k; i += blockDim.x) {
+        const float v = __uint_as_float(static_cast<uint32_t>(xr[i]) << 16);
+        const float g = __uint_as_float(static_cast<uint32_t>(gamma[i]) << 16);
+        xhat[row * k + i] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(__fmul_rn(v, r), g)));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// the projection
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(PB_THREADS, 1)
+    prefill_bf16_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+                        const PrefillBf16Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full[PB_STAGES], empty[PB_STAGES], tfull[2], tempty[2];
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+
+    uint8_t *smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
+    const int t = threadIdx.x;
+    const int warp = t >> 5;
+    const int lane = t & 31;
+    const int nk = (p.k + PB_BK - 1) / PB_BK;
+
+    if (t == 0) {
+        abort_flag = 0;
+        for (int i = 0; i < PB_STAGES; ++i) {
+            mbar_init(&full[i], 1);   // the copy thread's expect_tx
+            mbar_init(&empty[i], 1);  // the MMA thread's commit
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull[i], 1);              // the MMA thread's commit
+            mbar_init(&tempty[i], PB_EPI_WARPS);  // one arrival per epilogue warp
+        }
+    }
+    if (warp == PB_MMA_WARP) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&tmem_base)),
+                     "r"(2 * PB_BN)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    pdl_trigger();
+    pdl_wait();  // x_hat comes from the previous kernel
+    const uint32_t tmem = tmem_base;
+
+    if (warp == PB_TMA_WARP) {
+        // ---------------- copies: x_hat slab and the two weight slabs per K step
+        if (lane == 0) {
+            uint32_t it = 0;
+            int64_t last = -1;
+            bool ok = true;
+            for (int64_t tile = blockIdx.x; ok && tile < p.tiles; tile += gridDim.x) {
+                const int64_t mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+                const int m0 = static_cast<int>(mt * PB_BM);
+                const int r0 = static_cast<int>(p.silu ? nt * 128 : nt * PB_BN);
+                const int r1 = static_cast<int>(p.silu ? p.half + nt * 128 : nt * PB_BN + 128);
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const uint32_t s = it % PB_STAGES, use = it / PB_STAGES;
+                    if (!(ok = tc_wait(&empty[s], (use & 1) ^ 1, &abort_flag))) break;
+                    mbar_expect_tx(&full[s], PB_STAGE);
+                    uint8_t *a = smem + s * PB_STAGE;
+                    uint8_t *b = a + PB_A_BYTES;
+                    tma_load_2d(a, &tma_a, kb * PB_BK, m0, &full[s]);
+                    tma_load_2d(b, &tma_b, kb * PB_BK, r0, &full[s]);
+                    tma_load_2d(b + PB_B_BYTES / 2, &tma_b, kb * PB_BK, r1, &full[s]);
+                    last = it;
+                }
+            }
+            // After an abort the last copies may still be landing: let them finish
+            // (bounded) before the CTA's shared memory goes away.
+            if (!ok && last >= 0) mbar_wait_bounded(&full[last % PB_STAGES], (last / PB_STAGES) & 1, kCopyWaitLimitNs);
+        }
+        __syncwarp();
+    } else if (warp == PB_MMA_WARP) {
+        // ---------------- MMA issue: four K = 16 steps per stage ------------------
+        if (lane == 0) {
+            // D f32, A and B bf16, both K-major, N = 256, M = 128
+            const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(PB_BN >> 3) << 17) |
+                                   (static_cast<uint32_t>(PB_BM >> 4) << 24);
+            uint32_t it = 0, tc = 0;
+            int64_t last = -1;  // last stage whose MMAs were issued
+            bool ok = true;
+            for (int64_t tile = blockIdx.x; ok && tile < p.tiles; tile += gridDim.x, ++tc) {
+                const uint32_t buf = tc & 1, tuse = tc >> 1;
+                if (!(ok = tc_wait(&tempty[buf], (tuse & 1) ^ 1, &abort_flag))) break;
+                tc_fence_after();
+                const uint32_t d = tmem + buf * PB_BN;
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const uint32_t s = it % PB_STAGES, use = it / PB_STAGES;
+                    if (!(ok = tc_wait(&full[s], use & 1, &abort_flag))) break;
+                    tc_fence_after();
+                    const uint32_t a = smem_addr(smem + s * PB_STAGE);
+                    const uint32_t b = a + PB_A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < PB_BK / 16; ++kk)
+                        umma_f16(d, umma_desc_sw128(a + 32 * kk), umma_desc_sw128(b + 32 * kk), idesc,
+                                 (kb | kk) != 0 ? 1u : 0u);
+                    umma_commit(&empty[s]);
+                    last = it;
+                }
+                if (!ok) break;
+                umma_commit(&tfull[buf]);
+            }
+            // After an abort, wait (bounded) for the last issued MMAs before TMEM is freed.
+            if (!ok && last >= 0) mbar_wait_bounded(&empty[last % PB_STAGES], (last / PB_STAGES) & 1, kCopyWaitLimitNs);
+        }
+        __syncwarp();
+    } else if (warp < PB_EPI_WARPS) {
+        // ---------------- epilogue: warp w reads TMEM lanes (tile rows) 32 w .. +31
+        const int row = warp * 32 + lane;
+        const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+        const bool vec = (p.n_out % 4) == 0;
+        uint32_t tc = 0;
+        bool ok = true;
+        for (int64_t tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++tc) {
+            const uint32_t buf = tc & 1, tuse = tc >> 1;
+            // tcgen05.ld is warp-collective: the whole warp proceeds or stops
+            ok = ok && __all_sync(0xffffffffu, tc_wait(&tfull[buf], tuse & 1, &abort_flag));
+            tc_fence_after();
+            const int64_t mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+            const int64_t m = mt * PB_BM + row;
+            const int64_t n0 = nt * p.n_per_tile;
+            float *dst = p.y + m * p.n_out + n0;
+            const uint32_t ta = tmem + lane_addr + buf * PB_BN;
+            for (int c0 = 0; c0 < p.n_per_tile; c0 += 32) {
+                uint32_t a[32], b[32];
+                float v[32];
+                if (ok) {
+                    tmem_ld_32(ta + c0, a);
+                    if (p.silu) tmem_ld_32(ta + 128 + c0, b);
+                    tmem_ld_wait();
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    v[j] = !ok ? __int_as_float(0x7fc00000)
+                               : p.silu ? silu_mul(__uint_as_float(a[j]), __uint_as_float(b[j])) : __uint_as_float(a[j]);
+                if (m < p.m) {
+                    if (vec && n0 + c0 + 32 <= p.n_out) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<float4 *>(dst + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (n0 + c0 + j < p.n_out) dst[c0 + j] = v[j];
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[buf]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == PB_MMA_WARP) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * PB_BN) : "memory");
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+// TMA needs 16-byte row strides: k a multiple of 8.
+bool prefill_bf16_supported(int64_t k) { return k > 0 && k % 8 == 0; }
+
+static cudaError_t bf16_map(EncodeTiledFn enc, CUtensorMap *map, const uint16_t *base, int64_t rows, int64_t k)
+{
+    const cuuint64_t dim[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t stride[1] = {static_cast<cuuint64_t>(k) * 2};
+    const cuuint32_t box[2] = {PB_BK, 128};
+    const cuuint32_t estride[2] = {1, 1};
+    if (enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(base), dim, stride, box, estride,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    return cudaSuccess;
+}
+
+cudaError_t launch_prefill_bf16(const uint16_t *w, int64_t n_rows, int64_t k, const uint16_t *x, int64_t m,
+                                const uint16_t *gamma, float eps, int epi, uint16_t *xhat, float *y, cudaStream_t s)
+{
+    if (m == 0 || n_rows == 0) return cudaSuccess;
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return cudaErrorNotSupported;
+    const uint16_t *a = x;
+    if (gamma) {
+        const float inv_k = 1.0f / static_cast<float>(k);
+        if (cudaError_t e = launch_pdl(rmsnorm_bf16_rows_kernel, dim3(static_cast<unsigned>(m)), dim3(256), 0, s, x,
+                                       gamma, static_cast<int>(k), inv_k, eps, xhat);
+            e != cudaSuccess)
+            return e;
+        a = xhat;
+    }
+    CUtensorMap amap, bmap;
+    if (cudaError_t e = bf16_map(enc, &amap, a, m, k); e != cudaSuccess) return e;
+    if (cudaError_t e = bf16_map(enc, &bmap, w, n_rows, k); e != cudaSuccess) return e;
+    PrefillBf16Params p;
+    p.y = y;
+    p.m = m;
+    p.silu = epi == QG_EPI_SILU_MUL_HALVES ? 1 : 0;
+    p.half = n_rows / 2;
+    p.n_out = p.silu ? p.half : n_rows;
+    p.k = static_cast<int>(k);
+    p.n_per_tile = p.silu ? 128 : PB_BN;
+    p.m_tiles = (m + PB_BM - 1) / PB_BM;
+    p.tiles = p.m_tiles * ((p.n_out + p.n_per_tile - 1) / p.n_per_tile);
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(prefill_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PB_SMEM);
+    });
+    if (attr != cudaSuccess) return attr;
+    const int64_t grid = p.tiles < num_sms() ? p.tiles : num_sms();
+    return launch_pdl(prefill_bf16_kernel, dim3(static_cast<unsigned>(grid)), dim3(PB_THREADS), PB_SMEM, s, amap,
+                      bmap, p);
+}
+
+}  // namespace qg

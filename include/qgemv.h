@@ -358,6 +358,34 @@ QG_API qg_status qg_debug_block_dots_q8_0(const int8_t *w_qs, int64_t n_rows, in
                                    const int8_t *xq, int64_t batch, int32_t *s,
                                    qg_stream_t stream);
 
+/*
+ * qgemm_bf16_prefill - qgemv_bf16 for m prompt rows at once, on the tcgen05
+ * tensor cores ([Herbert] The numerical contract: bf16 weights and activations,
+ * f32 accumulators; Emitting for a GPU: norm fused in front, SiLU(g)*u behind,
+ * stacked gate|up; [Phobos] Fast Decode: a prompt reuses every weight for all of
+ * its rows, so it runs on the tensor cores).  Row i of the result is what
+ * qgemv_bf16 computes for row i of x, up to the order of the f32 sums:
+ *   with gamma != NULL, per row: r = 1/sqrt(mean(x^2)+eps) (f64, rounded to f32),
+ *   x_hat = bf16_rne((x * r) * gamma); with gamma == NULL, x_hat = x;
+ *   acc[i][n] = sum_k f32(w[n][k]) * f32(x_hat[i][k]) in f32 (exact products);
+ *   epilogue QG_EPI_NONE (y[i][n] = acc, n_out = n_rows) or
+ *   QG_EPI_SILU_MUL_HALVES (y[i][j] = silu(acc[i][j]) * acc[i][j + n_rows/2],
+ *   n_out = n_rows / 2, n_rows even).
+ *   w: device bf16 bits [n_rows][k] (read), 16-byte aligned; k a multiple of 8,
+ *      k <= 16384
+ *   x: device bf16 bits [m][k] (read), 16-byte aligned; gamma: bf16 bits [k] or NULL
+ *   xhat: device bf16 [m][k] work buffer, owned by the caller, written when
+ *      gamma != NULL (may be NULL otherwise), 16-byte aligned, not overlapping x
+ *   y: device f32 [m][n_out] (written), 16-byte aligned; m <= 2^24
+ *   Runs one CTA per SM over 128 x 256 accumulator tiles.  If an operand copy
+ *   stalls beyond one second the kernel stops waiting and writes NaN for the
+ *   tiles it has left, rather than hanging.  Errors: QG_ERR_SHAPE, QG_ERR_NULL,
+ *   QG_ERR_ALIGN, QG_ERR_UNSUPPORTED (epilogue QG_EPI_RESIDUAL_ADD), QG_ERR_CUDA.
+ */
+QG_API qg_status qgemm_bf16_prefill(const uint16_t *w, int64_t n_rows, int64_t k, const uint16_t *x,
+                                    int64_t m, const uint16_t *gamma, float eps, int epilogue,
+                                    uint16_t *xhat, float *y, qg_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

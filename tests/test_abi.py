@@ -188,3 +188,18 @@ def test_noalloc_stack_argument_errors(lib):
     assert f(FAKE, FAKE, 1, arr, nul, arr, arr, arr, 1024, 3584, eps, None) == 1
     assert f(FAKE + 4, FAKE, 1, arr, arr, arr, arr, arr, 1024, 3584, eps, None) == 2
     assert f(None, FAKE, 0, None, None, None, None, None, 1024, 3584, eps, None) == 1
+
+
+def test_bf16_prefill_argument_errors(lib):
+    """qgemm_bf16_prefill refuses bad requests before anything is launched."""
+    q = lib.qgemm_bf16_prefill
+    e = ctypes.c_float(1e-6)
+    # w, n_rows, k, x, m, gamma, eps, epilogue, xhat, y, stream
+    assert q(FAKE, 8, 12, FAKE, 4, None, e, 0, None, FAKE, None) == 3      # k not a multiple of 8
+    assert q(FAKE, 8, 16, FAKE, -1, None, e, 0, None, FAKE, None) == 3     # negative m
+    assert q(FAKE, 7, 16, FAKE, 4, None, e, 1, None, FAKE, None) == 3      # odd rows for SiLU(g)*u
+    assert q(FAKE, 8, 16, FAKE, 4, None, e, 2, None, FAKE, None) == 4      # residual epilogue not served
+    assert q(FAKE, 8, 16, FAKE, 4, FAKE, e, 0, None, FAKE, None) == 1      # gamma without its work buffer
+    assert q(FAKE + 8, 8, 16, FAKE, 4, None, e, 0, None, FAKE, None) == 2  # weights not 16-byte aligned
+    assert q(FAKE, 8, 16, FAKE, 4, FAKE, e, 0, FAKE, FAKE, None) == 3      # work buffer overlaps x
+    assert q(None, 0, 16, None, 4, None, e, 0, None, None, None) == 0      # no rows: nothing to do

@@ -208,3 +208,62 @@ def test_prefill_tc_matches_mma_sync_path(torch, orc):
     xq, xdo = orc.quantize_q8_0(x)
     _, a64 = orc.gemv_q8_0(qs, d, xq, xdo)
     assert_close(y1, ym, a64, 2 * TOL_Q8, "tc vs mma.sync")
+
+
+# ---------------------------------------------------------------------------
+# bf16 projection for a whole prompt on the tensor cores
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("m,n,k,norm,epi", [
+    (512, 18432, 2560, True, "silu_mul"),  # 4B-shaped gate|up for a 512-row prompt (rows sampled)
+    (3, 256, 64, True, "none"),
+    (130, 520, 2560, True, "silu_mul"),    # ragged M tile, ragged last output tile (half = 260)
+    (200, 300, 1000, False, "none"),       # k not a multiple of 64: zeros past the row end
+    (129, 512, 4104, True, "none"),
+    (1, 2, 8, True, "silu_mul"),           # smallest shape
+])
+def test_bf16_prefill(torch, orc, m, n, k, norm, epi):
+    from block_quantized_decode_rmsnorm_gb300 import api
+
+    case = synth.bf16_case(m + n + k, n_rows=n, k=k)
+    xbits = synth.bf16_normal_bits(m + k, 7, (m, k))
+    gamma = case["gamma"] if norm else None
+    n_out = n // 2 if epi == "silu_mul" else n
+    gy = Guarded(torch, (m, n_out), torch.float32)
+    xhat = torch.empty((m, k), dtype=torch.bfloat16, device="cuda") if norm else None
+    api.qgemm_bf16_prefill(_bf16(case["w"], torch), _bf16(xbits, torch),
+                           None if gamma is None else _bf16(gamma, torch), EPS, epilogue=epi, y=gy.view, xhat=xhat)
+    torch.cuda.synchronize()
+    gy.check()
+    y = gy.view.cpu().numpy()
+    rows = range(m) if m * n * k <= 200 * 600 * 4104 else [0, 1, m // 2, m - 1]
+    for i in rows:
+        y64, a64, xh, _ = orc.gemv_bf16(case["w"], xbits[i], gamma, EPS)
+        if norm:  # the normalised row, bit for bit
+            assert np.array_equal(xhat[i].view(torch.int16).cpu().numpy().view(np.uint16), xh), f"x_hat row {i}"
+        if epi == "silu_mul":
+            F = n // 2
+            g, u = y64[:F], y64[F:]
+            assert_close(y[i], orc.silu_mul(g, u), silu_scale(g, u, a64[:F], a64[F:], TOL_BF16), TOL_BF16,
+                         f"row {i} silu")
+        else:
+            assert_close(y[i], y64, a64, TOL_BF16, f"row {i}")
+
+
+def test_bf16_prefill_rows_match_gemv(torch, orc):
+    """Each prompt row equals the decode GEMV of that row (same x_hat bits, the
+    same f32 products, only the summation order differs)."""
+    from block_quantized_decode_rmsnorm_gb300 import api
+
+    m, n, k = 64, 1024, 1024
+    case = synth.bf16_case(91, n_rows=n, k=k)
+    xbits = synth.bf16_normal_bits(92, 7, (m, k))
+    w, g = _bf16(case["w"], torch), _bf16(case["gamma"], torch)
+    x = _bf16(xbits, torch)
+    y = api.qgemm_bf16_prefill(w, x, g, EPS, epilogue="silu_mul").cpu().numpy()
+    for i in (0, 17, 63):
+        yr = api.qgemv_bf16(w, x[i].contiguous(), g, EPS, epilogue="silu_mul").cpu().numpy()
+        y64, a64, _, _ = orc.gemv_bf16(case["w"], xbits[i], case["gamma"], EPS)
+        F = n // 2
+        scale = silu_scale(y64[:F], y64[F:], a64[:F], a64[F:], TOL_BF16)
+        assert_close(y[i], yr.astype(np.float64), scale, 2 * TOL_BF16, f"row {i} vs gemv")
