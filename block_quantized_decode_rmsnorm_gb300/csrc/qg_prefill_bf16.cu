@@ -19,8 +19,10 @@
 //  * one thread issues four tcgen05.mma kind::f16 (bf16 A and B, M = 128,
 //    N = 256, K = 16) per stage into a TMEM accumulator (two of 256 columns, so
 //    the epilogue of one tile overlaps the main loop of the next);
-//  * four epilogue warps read the accumulator with tcgen05.ld and store f32
-//    outputs (SiLU(g) * u from the two halves where asked).
+//  * eight epilogue warps (two per TMEM lane quarter, each half of the
+//    columns) read the accumulator with tcgen05.ld and store f32 outputs
+//    (SiLU(g) * u from the two halves where asked, with the fast exponential
+//    and division: a few ulp, far inside the bf16 contract's tolerance).
 // Products of bf16 values are exact in f32 and the MMA accumulates in f32, as
 // the numerical contract asks; only the summation order differs from a GEMV.
 // Every barrier wait is bounded by the global timer; a stalled pipeline aborts
@@ -42,10 +44,10 @@ constexpr int PB_A_BYTES = PB_BM * PB_BK * 2;        // 16 KB
 constexpr int PB_B_BYTES = PB_BN * PB_BK * 2;        // 32 KB
 constexpr int PB_STAGE = PB_A_BYTES + PB_B_BYTES;    // 48 KB, a multiple of 1024
 constexpr int PB_SMEM = PB_STAGES * PB_STAGE + 1024; // + alignment of the base
-constexpr int PB_EPI_WARPS = 4;
-constexpr int PB_TMA_WARP = 4;
-constexpr int PB_MMA_WARP = 5;
-constexpr int PB_THREADS = 6 * 32;
+constexpr int PB_EPI_WARPS = 8;  // two per TMEM lane quarter, each half of the columns
+constexpr int PB_TMA_WARP = 8;
+constexpr int PB_MMA_WARP = 9;
+constexpr int PB_THREADS = 10 * 32;
 
 struct PrefillBf16Params {
     float *y;         // [m][n_out]
@@ -62,24 +64,64 @@ struct PrefillBf16Params {
 // ---------------------------------------------------------------------------
 // x_hat for every prompt row
 // ---------------------------------------------------------------------------
-// One CTA per row: r from the compensated sum of exact squares (as in the GEMV),
-// then x_hat = bf16((x * r) * gamma), two f32 roundings and one bf16 rounding.
-__global__ void __launch_bounds__(256) rmsnorm_bf16_rows_kernel(const uint16_t *x, const uint16_t *gamma, int k,
-                                                                float inv_k, float eps, uint16_t *xhat)
+// One CTA per row: the row is read once in 16-byte pieces kept in registers;
+// r from the compensated sum of exact squares (as in the GEMV), then
+// x_hat = bf16((x * r) * gamma), two f32 roundings and one bf16 rounding.
+constexpr int NR_THREADS = 128;
+constexpr int NR_MAXC = 16;  // 16-byte pieces per thread: k <= 16384
+__global__ void __launch_bounds__(NR_THREADS) rmsnorm_bf16_rows_kernel(const uint16_t *x, const uint16_t *gamma,
+                                                                       int k, float inv_k, float eps, uint16_t *xhat)
 {
-    __shared__ float scratch[2 * 8 + 1];
+    __shared__ float scratch[2 * (NR_THREADS / 32) + 1];
     const int64_t row = blockIdx.x;
-    const uint16_t *xr = x + row * k;
+    const int nc = k / 8;
+    const uint4 *xr = reinterpret_cast<const uint4 *>(x + row * k);
     pdl_trigger();
     pdl_wait();
+    uint4 v[NR_MAXC];
     f32pair acc = {0.0f, 0.0f};
-    for (int i = threadIdx.x; i < k; i += blockDim.x) pair_add_square(acc, __uint_as_float(static_cast<uint32_t>(xr[i]) << 16));
-    const float r = block_rms_inv(acc, k, inv_k, eps, scratch);
-    for (int i = threadIdx.x; i < k; i += blockDim.x) {
-        const float v = __uint_as_float(static_cast<uint32_t>(xr[i]) << 16);
-        const float g = __uint_as_float(static_cast<uint32_t>(gamma[i]) << 16);
-        xhat[row * k + i] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(__fmul_rn(v, r), g)));
+#pragma unroll
+    for (int j = 0; j < NR_MAXC; ++j) {
+        const int c = static_cast<int>(threadIdx.x) + NR_THREADS * j;
+        if (c < nc) {
+            v[j] = xr[c];
+            const uint32_t u[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                pair_add_square(acc, __uint_as_float(u[i] << 16));
+                pair_add_square(acc, __uint_as_float(u[i] & 0xffff0000u));
+            }
+        }
     }
+    const float r = block_rms_inv(acc, k, inv_k, eps, scratch);
+    uint4 *out = reinterpret_cast<uint4 *>(xhat + row * k);
+    const uint4 *gr = reinterpret_cast<const uint4 *>(gamma);
+#pragma unroll
+    for (int j = 0; j < NR_MAXC; ++j) {
+        const int c = static_cast<int>(threadIdx.x) + NR_THREADS * j;
+        if (c < nc) {
+            const uint4 g4 = gr[c];
+            const uint32_t u[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+            const uint32_t gu[4] = {g4.x, g4.y, g4.z, g4.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float lo = __fmul_rn(__fmul_rn(__uint_as_float(u[i] << 16), r), __uint_as_float(gu[i] << 16));
+                const float hi = __fmul_rn(__fmul_rn(__uint_as_float(u[i] & 0xffff0000u), r),
+                                           __uint_as_float(gu[i] & 0xffff0000u));
+                o[i] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+                       (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+            }
+            out[c] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+}
+
+// silu(g) * u = g u / (1 + e^-g) with the fast exponential and division (a few
+// ulp; for g below about -88, e^-g is infinite and the quotient is 0).
+__device__ __forceinline__ float silu_mul_fast(float g, float u)
+{
+    return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
 // ---------------------------------------------------------------------------
@@ -187,9 +229,13 @@ __global__ void __launch_bounds__(PB_THREADS, 1)
         }
         __syncwarp();
     } else if (warp < PB_EPI_WARPS) {
-        // ---------------- epilogue: warp w reads TMEM lanes (tile rows) 32 w .. +31
-        const int row = warp * 32 + lane;
-        const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+        // ---------------- epilogue: warp w reads TMEM lanes (tile rows)
+        // 32 (w % 4) .. +31 and half w / 4 of the tile's columns
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+        const int cw = p.n_per_tile / 2;  // output columns per warp
+        const int cbeg = (warp >> 2) * cw;
         const bool vec = (p.n_out % 4) == 0;
         uint32_t tc = 0;
         bool ok = true;
@@ -203,7 +249,7 @@ __global__ void __launch_bounds__(PB_THREADS, 1)
             const int64_t n0 = nt * p.n_per_tile;
             float *dst = p.y + m * p.n_out + n0;
             const uint32_t ta = tmem + lane_addr + buf * PB_BN;
-            for (int c0 = 0; c0 < p.n_per_tile; c0 += 32) {
+            for (int c0 = cbeg; c0 < cbeg + cw; c0 += 32) {
                 uint32_t a[32], b[32];
                 float v[32];
                 if (ok) {
@@ -214,7 +260,7 @@ __global__ void __launch_bounds__(PB_THREADS, 1)
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
                     v[j] = !ok ? __int_as_float(0x7fc00000)
-                               : p.silu ? silu_mul(__uint_as_float(a[j]), __uint_as_float(b[j])) : __uint_as_float(a[j]);
+                               : p.silu ? silu_mul_fast(__uint_as_float(a[j]), __uint_as_float(b[j])) : __uint_as_float(a[j]);
                 if (m < p.m) {
                     if (vec && n0 + c0 + 32 <= p.n_out) {
 #pragma unroll
@@ -269,7 +315,7 @@ cudaError_t launch_prefill_bf16(const uint16_t *w, int64_t n_rows, int64_t k, co
     const uint16_t *a = x;
     if (gamma) {
         const float inv_k = 1.0f / static_cast<float>(k);
-        if (cudaError_t e = launch_pdl(rmsnorm_bf16_rows_kernel, dim3(static_cast<unsigned>(m)), dim3(256), 0, s, x,
+        if (cudaError_t e = launch_pdl(rmsnorm_bf16_rows_kernel, dim3(static_cast<unsigned>(m)), dim3(NR_THREADS), 0, s, x,
                                        gamma, static_cast<int>(k), inv_k, eps, xhat);
             e != cudaSuccess)
             return e;
