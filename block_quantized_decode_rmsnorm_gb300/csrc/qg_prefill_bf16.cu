@@ -22,7 +22,9 @@
 //  * eight epilogue warps (two per TMEM lane quarter, each half of the
 //    columns) read the accumulator with tcgen05.ld and store f32 outputs
 //    (SiLU(g) * u from the two halves where asked, with the fast exponential
-//    and division: a few ulp, far inside the bf16 contract's tolerance).
+//    and division: a few ulp, far inside the bf16 contract's tolerance); each
+//    warp turns its 32 x 32 blocks around in shared memory so that every store
+//    instruction writes 128 contiguous bytes of one output row.
 // Products of bf16 values are exact in f32 and the MMA accumulates in f32, as
 // the numerical contract asks; only the summation order differs from a GEMV.
 // Every barrier wait is bounded by the global timer; a stalled pipeline aborts
@@ -43,8 +45,9 @@ constexpr int PB_STAGES = 4;
 constexpr int PB_A_BYTES = PB_BM * PB_BK * 2;        // 16 KB
 constexpr int PB_B_BYTES = PB_BN * PB_BK * 2;        // 32 KB
 constexpr int PB_STAGE = PB_A_BYTES + PB_B_BYTES;    // 48 KB, a multiple of 1024
-constexpr int PB_SMEM = PB_STAGES * PB_STAGE + 1024; // + alignment of the base
+constexpr int PB_XPOSE = 32 * 33 * 4;                // per epilogue warp: a padded 32 x 32 f32 block
 constexpr int PB_EPI_WARPS = 8;  // two per TMEM lane quarter, each half of the columns
+constexpr int PB_SMEM = PB_STAGES * PB_STAGE + PB_EPI_WARPS * PB_XPOSE + 1024; // + alignment of the base
 constexpr int PB_TMA_WARP = 8;
 constexpr int PB_MMA_WARP = 9;
 constexpr int PB_THREADS = 10 * 32;
@@ -232,11 +235,10 @@ __global__ void __launch_bounds__(PB_THREADS, 1)
         // ---------------- epilogue: warp w reads TMEM lanes (tile rows)
         // 32 (w % 4) .. +31 and half w / 4 of the tile's columns
         const int q = warp & 3;
-        const int row = q * 32 + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
         const int cw = p.n_per_tile / 2;  // output columns per warp
         const int cbeg = (warp >> 2) * cw;
-        const bool vec = (p.n_out % 4) == 0;
+        float *xp = reinterpret_cast<float *>(smem + PB_STAGES * PB_STAGE + warp * PB_XPOSE);  // [32][33]
         uint32_t tc = 0;
         bool ok = true;
         for (int64_t tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++tc) {
@@ -245,9 +247,7 @@ __global__ void __launch_bounds__(PB_THREADS, 1)
             ok = ok && __all_sync(0xffffffffu, tc_wait(&tfull[buf], tuse & 1, &abort_flag));
             tc_fence_after();
             const int64_t mt = tile % p.m_tiles, nt = tile / p.m_tiles;
-            const int64_t m = mt * PB_BM + row;
             const int64_t n0 = nt * p.n_per_tile;
-            float *dst = p.y + m * p.n_out + n0;
             const uint32_t ta = tmem + lane_addr + buf * PB_BN;
             for (int c0 = cbeg; c0 < cbeg + cw; c0 += 32) {
                 uint32_t a[32], b[32];
@@ -261,16 +261,19 @@ __global__ void __launch_bounds__(PB_THREADS, 1)
                 for (int j = 0; j < 32; ++j)
                     v[j] = !ok ? __int_as_float(0x7fc00000)
                                : p.silu ? silu_mul_fast(__uint_as_float(a[j]), __uint_as_float(b[j])) : __uint_as_float(a[j]);
-                if (m < p.m) {
-                    if (vec && n0 + c0 + 32 <= p.n_out) {
+                // lane l holds row l of the block: through shared memory (row
+                // stride 33 floats, conflict-free both ways), then lane l stores
+                // column l of each row
+                __syncwarp();
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4)
-                            *reinterpret_cast<float4 *>(dst + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (n0 + c0 + j < p.n_out) dst[c0 + j] = v[j];
-                    }
+                for (int j = 0; j < 32; ++j) xp[lane * 33 + j] = v[j];
+                __syncwarp();
+                const int64_t m_base = mt * PB_BM + q * 32;
+                const bool col_ok = n0 + c0 + lane < p.n_out;
+#pragma unroll 8
+                for (int r = 0; r < 32; ++r) {
+                    const float val = xp[r * 33 + lane];
+                    if (m_base + r < p.m && col_ok) p.y[(m_base + r) * p.n_out + n0 + c0 + lane] = val;
                 }
             }
             tc_fence_before();
