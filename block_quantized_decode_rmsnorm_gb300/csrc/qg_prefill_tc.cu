@@ -89,7 +89,11 @@ struct TcLayout {
     static constexpr int OFF_W16 = XS * XSTAGE;
     static constexpr int OFF_W8 = OFF_W16 + TC_W_SLOTS * WSLOT_AL;
     static constexpr int OFF_DS = OFF_W8 + 2 * W8;
-    static constexpr int BYTES = OFF_DS + 2 * DS;
+    // BN = 64 only (the others leave no room): per epilogue warp a padded 32 x 17
+    // f32 block through which its tile rows are turned into row-contiguous stores
+    static constexpr bool XPOSE = BN == 64;
+    static constexpr int OFF_XP = OFF_DS + 2 * DS;
+    static constexpr int BYTES = OFF_XP + (XPOSE ? TC_EPI_WARPS * 32 * (BN / 4 + 1) * 4 : 0);
     static constexpr int CW = BN / 4;                      // columns per epilogue warp
     static_assert(BN % 32 == 0 && BN <= 128, "BN: a multiple of 32, at most 128");
     static_assert(2 * TMEM_BATCH <= TMEM_COLS, "two batches of block sums in TMEM");
@@ -360,14 +364,37 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     if (xi0 + B == TC_XB) mbar_arrive(&x_empty[xs]);
                 }
             }
+            if (!ok) {
+#pragma unroll
+                for (int i = 0; i < CW / 2; ++i) acc[i] = pack2(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
+            }
+            if constexpr (L::XPOSE) {
+                // lane l holds row l of the warp's 32 x 16 block: through shared
+                // memory, then each store writes 16 columns of two rows (64 bytes each)
+                float *xp = reinterpret_cast<float *>(smem + L::OFF_XP) + warp * 32 * (CW + 1);
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < CW / 2; ++i) {
+                    const float2 a = unpack2(acc[i]);
+                    xp[lane * (CW + 1) + 2 * i] = a.x;
+                    xp[lane * (CW + 1) + 2 * i + 1] = a.y;
+                }
+                __syncwarp();
+                const int hr = lane >> 4, col = lane & 15;
+                const bool col_ok = n0 + col0 + col < p.n;
+#pragma unroll 4
+                for (int r2 = 0; r2 < 32; r2 += 2) {
+                    const int64_t mr = mt * TC_BM + q * 32 + r2 + hr;
+                    const float v = xp[(r2 + hr) * (CW + 1) + col];
+                    if (mr < p.m && col_ok) p.y[mr * p.n + n0 + col0 + col] = v;
+                }
+                __syncwarp();  // the block is reused by the next tile
+                continue;
+            }
             const int64_t m = mt * TC_BM + row;
             if (m < p.m) {
                 float *dst = p.y + m * p.n + n0 + col0;
                 const bool full = (n0 + col0 + CW <= p.n) && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0);
-                if (!ok) {
-#pragma unroll
-                    for (int i = 0; i < CW / 2; ++i) acc[i] = pack2(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
-                }
                 if (full) {
 #pragma unroll
                     for (int i = 0; i < CW / 2; i += 2) {
