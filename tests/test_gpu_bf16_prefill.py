@@ -267,3 +267,34 @@ def test_bf16_prefill_rows_match_gemv(torch, orc):
         F = n // 2
         scale = silu_scale(y64[:F], y64[F:], a64[:F], a64[F:], TOL_BF16)
         assert_close(y[i], yr.astype(np.float64), scale, 2 * TOL_BF16, f"row {i} vs gemv")
+
+
+def test_bf16_prefill_deterministic_and_graph_replay(torch):
+    """The prompt projection sums in a fixed order: repeated calls and graph
+    replays give the same bits."""
+    from block_quantized_decode_rmsnorm_gb300 import api
+
+    m, n, k = 256, 1024, 2560
+    case = synth.bf16_case(93, n_rows=n, k=k)
+    w, g = _bf16(case["w"], torch), _bf16(case["gamma"], torch)
+    x = _bf16(synth.bf16_normal_bits(94, 7, (m, k)), torch)
+    xh = torch.empty((m, k), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((m, n // 2), dtype=torch.float32, device="cuda")
+    api.qgemm_bf16_prefill(w, x, g, EPS, epilogue="silu_mul", y=y, xhat=xh)
+    torch.cuda.synchronize()
+    want = y.cpu().numpy().copy()
+    api.qgemm_bf16_prefill(w, x, g, EPS, epilogue="silu_mul", y=y, xhat=xh)
+    torch.cuda.synchronize()
+    assert np.array_equal(y.cpu().numpy(), want)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            api.qgemm_bf16_prefill(w, x, g, EPS, epilogue="silu_mul", y=y, xhat=xh, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        y.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(y.cpu().numpy(), want)
