@@ -370,7 +370,14 @@ qg_status qgemm_bf16_prefill(const uint16_t *w, int64_t n_rows, int64_t k, const
     if (!w || !x || !y || (gamma && !xhat)) return QG_ERR_NULL;
     if (!aligned(w, 16) || !aligned(x, 16) || !aligned(gamma, 16) || !aligned(xhat, 16) || !aligned(y, 16))
         return QG_ERR_ALIGN;
-    if (gamma && overlap(x, xhat, static_cast<size_t>(m) * k * 2)) return QG_ERR_SHAPE;
+    // outputs (y, and xhat when written) must not overlap the inputs or each other
+    const size_t xb = static_cast<size_t>(m) * k * 2, wb = static_cast<size_t>(n_rows) * k * 2;
+    const size_t yb = static_cast<size_t>(m) * (epilogue == QG_EPI_SILU_MUL_HALVES ? n_rows / 2 : n_rows) * 4;
+    if (overlap(y, yb, x, xb) || overlap(y, yb, w, wb) || (gamma && overlap(y, yb, gamma, static_cast<size_t>(k) * 2)))
+        return QG_ERR_SHAPE;
+    if (gamma && (overlap(xhat, xb, x, xb) || overlap(xhat, xb, w, wb) || overlap(xhat, xb, y, yb) ||
+                  overlap(xhat, xb, gamma, static_cast<size_t>(k) * 2)))
+        return QG_ERR_SHAPE;
     return from_cuda(qg::launch_prefill_bf16(w, n_rows, k, x, m, gamma, eps, epilogue, xhat, y, stream));
 }
 

@@ -377,6 +377,8 @@ QG_API qg_status qg_debug_block_dots_q8_0(const int8_t *w_qs, int64_t n_rows, in
  *   xhat: device bf16 [m][k] work buffer, owned by the caller, written when
  *      gamma != NULL (may be NULL otherwise), 16-byte aligned, not overlapping x
  *   y: device f32 [m][n_out] (written), 16-byte aligned; m <= 2^24
+ *   Outputs (y, and xhat when gamma != NULL) must not overlap the inputs or
+ *   each other (QG_ERR_SHAPE).
  *   Runs one CTA per SM over 128 x 256 accumulator tiles.  If an operand copy
  *   stalls beyond one second the kernel stops waiting and writes NaN for the
  *   tiles it has left, rather than hanging.  Errors: QG_ERR_SHAPE, QG_ERR_NULL,

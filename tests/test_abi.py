@@ -202,4 +202,6 @@ def test_bf16_prefill_argument_errors(lib):
     assert q(FAKE, 8, 16, FAKE, 4, FAKE, e, 0, None, FAKE, None) == 1      # gamma without its work buffer
     assert q(FAKE + 8, 8, 16, FAKE, 4, None, e, 0, None, FAKE, None) == 2  # weights not 16-byte aligned
     assert q(FAKE, 8, 16, FAKE, 4, FAKE, e, 0, FAKE, FAKE, None) == 3      # work buffer overlaps x
+    assert q(FAKE, 8, 16, FAKE + 4096, 4, None, e, 0, None, FAKE + 4096, None) == 3  # y overlaps x
+    assert q(FAKE, 8, 16, FAKE + 4096, 4, FAKE + 8192, e, 0, FAKE + 16384, FAKE, None) == 3  # y overlaps w
     assert q(None, 0, 16, None, 4, None, e, 0, None, None, None) == 0      # no rows: nothing to do
