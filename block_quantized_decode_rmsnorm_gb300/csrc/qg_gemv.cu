@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_q8_0_reg_kernel(const GemvP
 }
 
 // ---------------------------------------------------------------------------
-// Batched GEMV on the int8 tensor cores (batch 3..8, K a multiple of 256)
+// Batched GEMV on the int8 tensor cores (batch 2..8, K a multiple of 256)
 // ---------------------------------------------------------------------------
 // "Filling in the blanks: Inference using Phobos", GPU Performance Heisenbugs:
 // exact int8 values on the integer tensor cores.  One mma.sync.m16n8k32 (s8,
@@ -467,7 +467,7 @@ cudaError_t launch_gemv_q8_0(const int8_t *w_qs, const uint16_t *w_d, int64_t n_
     p.n_tasks = 0;
     p.batch = static_cast<int>(batch);
     const int nbl = (p.nb + 31) / 32;
-    if (batch >= 3 && epi != QG_EPI_SILU_MUL_HALVES && k % 256 == 0 && k <= 4096 &&
+    if (batch >= 2 && epi != QG_EPI_SILU_MUL_HALVES && k % 256 == 0 && k <= 4096 &&
         (reinterpret_cast<uintptr_t>(w_d) & 15) == 0) {
         // tensor-core path: 16 rows per warp task, the batch's codes staged in shared memory
         const void *kern = reinterpret_cast<const void *>(gemv_q8_0_mma_kernel);

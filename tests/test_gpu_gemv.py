@@ -98,10 +98,10 @@ def test_gemv_residual_in_place(torch, orc):
 @pytest.mark.parametrize("batch", [2, 4])
 def test_stacked_equals_separate_and_batch_invariance(torch, orc, batch):
     """Stacked gate|up == the two separate products, bit for bit (same per-row
-    arithmetic).  Batch invariance: the register-tile kernel (batch 1, 2) gives
-    every batch row the same bits as a batch-1 call; the tensor-core kernel
-    (batch 3-8) gives each row the same bits at any batch it serves (here 4 vs
-    the same rows inside a batch of 8), and agrees with batch 1 to the tolerance."""
+    arithmetic).  Batch invariance: the tensor-core kernel (batch 2-8) gives each
+    row the same bits at any batch it serves (here 2 and 4 against the same rows
+    inside a batch of twice the size), and agrees with the batch-1 register-tile
+    kernel to the tolerance."""
     from block_quantized_decode_rmsnorm_gb300 import api
 
     F, k = 3584, 1024
@@ -114,11 +114,8 @@ def test_stacked_equals_separate_and_batch_invariance(torch, orc, batch):
     y64, a64 = orc.gemv_q8_0(qs, d, xq, xd)
     for b in range(batch):
         y1 = api.qgemv_q8_0(weight(qs, d), xq_t[b:b + 1], xd_t[b:b + 1]).cpu().numpy()
-        if batch <= 2:
-            assert np.array_equal(y1[0], st[b])
-        else:
-            assert_close(y1[0], st[b], a64[b], 2 * TOL_Q8, "batch 1 vs tensor-core batch")
-    if batch > 2:
+        assert_close(y1[0], st[b], a64[b], 2 * TOL_Q8, "batch 1 vs tensor-core batch")
+    if batch > 1:
         xq8 = np.concatenate([xq, xq[::-1]])
         xd8 = np.concatenate([xd, xd[::-1]])
         st8 = api.qgemv_q8_0(weight(qs, d), to_dev(xq8, torch), to_dev(xd8, torch, torch.float16)).cpu().numpy()
