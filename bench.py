@@ -334,6 +334,18 @@ def extra_configs(torch, pk) -> dict:
     # prompt-sized contraction: tensor-core path (activation tiles, tcgen05) at
     # the library's tile width and at each fixed one, and the int8 mma.sync
     # path, on the same rotating weight copies
+    # the int8 mma.sync path's rate, the prompt contraction's second roofline
+    api.qg_measure_mma_s8(100)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    mops = api.qg_measure_mma_s8(20000)
+    e1.record()
+    torch.cuda.synchronize()
+    mma_tops = mops / (e0.elapsed_time(e1) / 1e3) / 1e12
+    out["mma_sync_s8_rate"] = {"TOPS": mma_tops, "int_ops": mops,
+                               "note": "independent m16n8k32 s8 MMAs on register operands, 4 CTAs per SM"}
+
     pc = synth.prefill_case(0)
     wp = api.q8_weight_from_numpy(pc["w_qs"], pc["w_d"])
     copies = l2_copies(torch, wp.nbytes)
@@ -351,7 +363,8 @@ def extra_configs(torch, pk) -> dict:
     for name, fn in variants:
         r = cold_and_warm(torch, fn, wps, wp.nbytes)
         tops = ops / (r["us"] / 1e6) / 1e12
-        out[name] = {**r, "TOPS": tops, "frac_f16_dense_peak": tops / pk["bf16_tflops"], "int_ops": ops}
+        out[name] = {**r, "TOPS": tops, "frac_f16_dense_peak": tops / pk["bf16_tflops"],
+                     "frac_mma_s8_rate": tops / mma_tops, "int_ops": ops}
     del wps
     torch.cuda.empty_cache()
     _ = np

@@ -268,6 +268,17 @@ def qgemm_q8_0_prefill_tc(w: Q8Weight, xt: ActTiles, y: torch.Tensor | None = No
     return y
 
 
+def qg_measure_mma_s8(iters: int, stream=None) -> int:
+    """Launch the int8 mma.sync rate kernel (time the stream around it); returns
+    the int-ops the launch performs."""
+    import ctypes
+
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ops = ctypes.c_int64(0)
+    _lib.call("qg_measure_mma_s8", int(iters), sink.data_ptr(), ctypes.addressof(ops), _stream_handle(stream))
+    return ops.value
+
+
 def qg_debug_block_dots_q8_0(w: Q8Weight, xq: torch.Tensor, s: torch.Tensor | None = None,
                              stream=None) -> torch.Tensor:
     """Exact int32 block sums s[batch, n_rows, k/32]."""

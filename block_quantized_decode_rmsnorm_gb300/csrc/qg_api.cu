@@ -38,6 +38,7 @@ cudaError_t launch_decode_layers_noalloc(const float *, float *, int, const floa
 cudaError_t launch_quantize_act_tiles(const float *, int64_t, int64_t, void *, cudaStream_t);
 bool prefill_tc_supported(int64_t k);
 bool prefill_bf16_supported(int64_t k);
+cudaError_t launch_mma_s8_rate(int64_t, int *, int64_t *, cudaStream_t);
 cudaError_t launch_prefill_bf16(const uint16_t *, int64_t, int64_t, const uint16_t *, int64_t, const uint16_t *, float,
                                 int, uint16_t *, float *, cudaStream_t);
 cudaError_t launch_prefill_tc(const int8_t *, const uint16_t *, int64_t, int64_t, const void *, int64_t, float *, int,
@@ -379,6 +380,13 @@ qg_status qgemm_bf16_prefill(const uint16_t *w, int64_t n_rows, int64_t k, const
                   overlap(xhat, xb, gamma, static_cast<size_t>(k) * 2)))
         return QG_ERR_SHAPE;
     return from_cuda(qg::launch_prefill_bf16(w, n_rows, k, x, m, gamma, eps, epilogue, xhat, y, stream));
+}
+
+qg_status qg_measure_mma_s8(int64_t iters, int32_t *sink, int64_t *ops, qg_stream_t stream)
+{
+    if (iters < 1 || iters > (int64_t(1) << 24)) return QG_ERR_SHAPE;
+    if (!sink || !ops) return QG_ERR_NULL;
+    return from_cuda(qg::launch_mma_s8_rate(iters, sink, ops, stream));
 }
 
 qg_status qg_debug_block_dots_q8_0(const int8_t *w_qs, int64_t n_rows, int64_t k, const int8_t *xq, int64_t batch,

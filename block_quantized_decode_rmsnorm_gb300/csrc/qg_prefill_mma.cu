@@ -249,4 +249,46 @@ cudaError_t launch_prefill_mma(const int8_t *w_qs, const uint16_t *w_d, int64_t 
     return launch_pdl(prefill_mma_kernel, grid, dim3(PF_THREADS), smem, s, p);
 }
 
+// ---------------------------------------------------------------------------
+// rate of the int8 mma.sync path, for the prompt contraction's second roofline
+// ---------------------------------------------------------------------------
+// Every warp runs `iters` rounds of eight independent m16n8k32 s8 MMAs (2 * 16 *
+// 8 * 32 int-ops each) on register operands; nothing is loaded, so the time is
+// the tensor pipe's.  The sums reach memory only through an impossible-looking
+// test, which keeps the compiler from dropping the MMAs.
+constexpr int MR_THREADS = 256;
+__global__ void __launch_bounds__(MR_THREADS) mma_s8_rate_kernel(int iters, int *sink)
+{
+    uint32_t a[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = 0x01010101u * static_cast<uint32_t>((threadIdx.x + i) & 7);
+    const uint32_t b0 = 0x01020304u ^ threadIdx.x, b1 = 0x05060708u ^ blockIdx.x;
+    int c[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) c[j][i] = 0;
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            asm volatile("mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                         "{%0,%1,%2,%3};"
+                         : "+r"(c[j][0]), "+r"(c[j][1]), "+r"(c[j][2]), "+r"(c[j][3])
+                         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+        }
+    }
+    int t = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) t += c[j][0] ^ c[j][1] ^ c[j][2] ^ c[j][3];
+    if (t == 0x7fffffff) *sink = t;
+}
+
+cudaError_t launch_mma_s8_rate(int64_t iters, int *sink, int64_t *ops, cudaStream_t s)
+{
+    const int64_t grid = static_cast<int64_t>(num_sms()) * 4;
+    *ops = grid * (MR_THREADS / 32) * iters * 8 * (2LL * 16 * 8 * 32);
+    mma_s8_rate_kernel<<<static_cast<unsigned>(grid), MR_THREADS, 0, s>>>(static_cast<int>(iters), sink);
+    return cudaGetLastError();
+}
+
 }  // namespace qg

@@ -359,6 +359,18 @@ QG_API qg_status qg_debug_block_dots_q8_0(const int8_t *w_qs, int64_t n_rows, in
                                    qg_stream_t stream);
 
 /*
+ * qg_measure_mma_s8 - times nothing itself: launches a grid (4 CTAs per SM) whose
+ * warps issue `iters` rounds of eight independent mma.sync.m16n8k32 s8 MMAs on
+ * register operands, the int8 tensor path that sm_103a offers ([Phobos] GPU
+ * Performance Heisenbugs: integer tensor cores), so that a caller timing the
+ * stream gets that path's rate, the second roofline of the prompt contraction.
+ *   iters: 1 .. 2^24; sink: device int32 (written only in an impossible case);
+ *   *ops (host): the int-ops the launch performs.  Errors: QG_ERR_SHAPE,
+ *   QG_ERR_NULL, QG_ERR_CUDA.
+ */
+QG_API qg_status qg_measure_mma_s8(int64_t iters, int32_t *sink, int64_t *ops, qg_stream_t stream);
+
+/*
  * qgemm_bf16_prefill - qgemv_bf16 for m prompt rows at once, on the tcgen05
  * tensor cores ([Herbert] The numerical contract: bf16 weights and activations,
  * f32 accumulators; Emitting for a GPU: norm fused in front, SiLU(g)*u behind,

@@ -205,3 +205,11 @@ def test_bf16_prefill_argument_errors(lib):
     assert q(FAKE, 8, 16, FAKE + 4096, 4, None, e, 0, None, FAKE + 4096, None) == 3  # y overlaps x
     assert q(FAKE, 8, 16, FAKE + 4096, 4, FAKE + 8192, e, 0, FAKE + 16384, FAKE, None) == 3  # y overlaps w
     assert q(None, 0, 16, None, 4, None, e, 0, None, None, None) == 0      # no rows: nothing to do
+
+
+def test_measure_mma_s8_argument_errors(lib):
+    ops = ctypes.c_int64(0)
+    assert lib.qg_measure_mma_s8(0, FAKE, ctypes.addressof(ops), None) == 3          # no rounds
+    assert lib.qg_measure_mma_s8((1 << 24) + 1, FAKE, ctypes.addressof(ops), None) == 3
+    assert lib.qg_measure_mma_s8(10, None, ctypes.addressof(ops), None) == 1          # no sink
+    assert lib.qg_measure_mma_s8(10, FAKE, None, None) == 1                           # nowhere to report
