@@ -80,8 +80,6 @@ __device__ __forceinline__ u32x8 ld_stream_32B(const void *p, uint64_t pol)
     return r;
 }
 
-__device__ __forceinline__ void prefetch_l2(const void *p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
-
 // 16 bytes of streamed, read-only data (weights): not kept in L1, with a
 // 256-byte L2 prefetch hint.  p must be 16-byte aligned.
 __device__ __forceinline__ uint4 ld_stream_16B(const void *p)
@@ -179,20 +177,6 @@ __device__ __forceinline__ float warp_max_abs(float v)
     const uint32_t m = __reduce_max_sync(0xffffffffu, nan ? 0u : __float_as_uint(a));
     const uint32_t all_nan = __reduce_and_sync(0xffffffffu, nan ? 1u : 0u);
     return all_nan ? __uint_as_float(0x7fffffffu) : __uint_as_float(m);
-}
-
-__device__ __forceinline__ float warp_max(float v)
-{
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-
-__device__ __forceinline__ double warp_sum_f64(double v)
-{
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
 }
 
 // Q8_0 code of one value given the block's f32 scale d: round half away from
