@@ -360,12 +360,29 @@ def extra_configs(torch, pk) -> dict:
         variants.append((f"prefill_512x7168x1024_tcgen05_bn{bn}",
                          lambda w, bn=bn: api.qgemm_q8_0_prefill_tc(w, xt, y=yp, tile_n=bn)))
     variants.append(("prefill_512x7168x1024_mma_sync", lambda w: api.qgemm_q8_0_prefill(w, xq, xd, y=yp)))
+    wbytes = {}
+    for name, _ in variants:
+        wbytes[name] = (wps, wp.nbytes)
+    # wide-tile form: weights packed once to binary16 codes + block-major scales
+    wps2 = [api.qg_q8_0_pack_f16(w) for w in wps]
+    x2 = api.quantize_act_q8_0_f16(xdev)
+    w2bytes = wps2[0].codes.numel() * 2 + wps2[0].scales_t.numel() * 4
+    tc2 = [("prefill_512x7168x1024_tcgen05_wide", lambda w: api.qgemm_q8_0_prefill_tc2(w, x2, y=yp)),
+           ("prefill_512x7168x1024_tcgen05_wide_with_act_quant",
+            lambda w: api.qgemm_q8_0_prefill_tc2(w, api.quantize_act_q8_0_f16(xdev, out=x2), y=yp))]
+    for bn in (128, 192):
+        tc2.append((f"prefill_512x7168x1024_tcgen05_wide_bn{bn}",
+                    lambda w, bn=bn: api.qgemm_q8_0_prefill_tc2(w, x2, y=yp, tile_n=bn)))
+    for name, _ in tc2:
+        wbytes[name] = (wps2, w2bytes)
+    variants += tc2
     for name, fn in variants:
-        r = cold_and_warm(torch, fn, wps, wp.nbytes)
+        ws_, nb_ = wbytes[name]
+        r = cold_and_warm(torch, fn, ws_, nb_)
         tops = ops / (r["us"] / 1e6) / 1e12
         out[name] = {**r, "TOPS": tops, "frac_f16_dense_peak": tops / pk["bf16_tflops"],
                      "frac_mma_s8_rate": tops / mma_tops, "int_ops": ops}
-    del wps
+    del wps, wps2
     torch.cuda.empty_cache()
     _ = np
     return out
@@ -578,6 +595,13 @@ def run_workload(args):
         y = torch.empty((pc["x"].shape[0], pc["w_qs"].shape[0]), dtype=torch.float32, device="cuda")
         fn = lambda: api.qgemm_q8_0_prefill_tc(wt, xt, y=y)
         name = "prompt contraction 512x7168x1024, tcgen05"
+    elif w == "prefill_wide":
+        pc = synth.prefill_case(0)
+        w2 = api.qg_q8_0_pack_f16(api.q8_weight_from_numpy(pc["w_qs"], pc["w_d"]))
+        x2 = api.quantize_act_q8_0_f16(torch.from_numpy(pc["x"]).cuda())
+        y = torch.empty((pc["x"].shape[0], pc["w_qs"].shape[0]), dtype=torch.float32, device="cuda")
+        fn = lambda: api.qgemm_q8_0_prefill_tc2(w2, x2, y=y)
+        name = "prompt contraction 512x7168x1024, tcgen05 wide tiles"
     elif w.startswith("head"):
         b = int(w[4:])
         qs, d = synth.q8_0_weight_planes(0, synth.S_W0, 262144, 1024)
@@ -671,7 +695,7 @@ def main():
     ap.add_argument("--path", choices=["one", "two", "four"], default="two",
                     help="launches per decode layer: one (split-K down inside the layer kernel), two, four")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--workload", choices=["prefill", "prefill_bf16", "head1", "head2", "head4", "head8", "bf16"],
+    ap.add_argument("--workload", choices=["prefill", "prefill_wide", "prefill_bf16", "head1", "head2", "head4", "head8", "bf16"],
                     help="time one workload's kernel alone (for profiling) instead of the bench step")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -45,6 +45,10 @@ SIGNATURES = {
     "qg_decode_layers_q8_0_noalloc": (ST, [P, P, I32, P, P, P, P, P, I64, I64, F32, P]),
     "qg_debug_block_dots_q8_0": (ST, [P, I64, I64, P, I64, P, P]),
     "qg_measure_mma_s8": (ST, [I64, P, P, P]),
+    "qg_scales_ld": (I64, [I64]),
+    "qg_q8_0_pack_f16": (ST, [P, P, I64, I64, P, P, P]),
+    "quantize_act_q8_0_f16": (ST, [P, I64, I64, P, P, P]),
+    "qgemm_q8_0_prefill_tc2": (ST, [P, P, I64, I64, P, P, I64, P, I32, P]),
 }
 
 _lib = None

@@ -268,6 +268,78 @@ def qgemm_q8_0_prefill_tc(w: Q8Weight, xt: ActTiles, y: torch.Tensor | None = No
     return y
 
 
+@dataclass
+class F16Codes:
+    """Q8_0 operand of qgemm_q8_0_prefill_tc2: codes as binary16 ``torch.float16
+    [rows, k]`` (exact integers) and scales as ``torch.float32 [k/32, ld]``, ld =
+    rows rounded up to a multiple of four (columns past ``rows`` are padding)."""
+
+    codes: torch.Tensor
+    scales_t: torch.Tensor
+
+    @property
+    def rows(self) -> int:
+        return self.codes.shape[0]
+
+    @property
+    def k(self) -> int:
+        return self.codes.shape[1]
+
+    @classmethod
+    def empty(cls, rows: int, k: int, device) -> "F16Codes":
+        return cls(torch.empty((rows, k), dtype=torch.float16, device=device),
+                   torch.empty((k // 32, (rows + 3) // 4 * 4), dtype=torch.float32, device=device))
+
+    def check(self, name: str) -> None:
+        _need(self.codes, f"{name}.codes", torch.float16)
+        _need(self.scales_t, f"{name}.scales_t", torch.float32, (self.k // 32, (self.rows + 3) // 4 * 4))
+
+
+def qg_q8_0_pack_f16(w: Q8Weight, out: F16Codes | None = None, stream=None) -> F16Codes:
+    """Packed Q8_0 weight -> binary16 codes and block-major f32 scales."""
+    _need(w.qs, "w.qs", torch.int8)
+    n_rows, k = w.qs.shape
+    _need(w.d, "w.d", torch.float16, (n_rows, k // 32))
+    if out is None:
+        out = F16Codes.empty(n_rows, k, w.qs.device)
+    out.check("out")
+    if (out.rows, out.k) != (n_rows, k):
+        raise ValueError("qg_q8_0_pack_f16: output of another shape")
+    _lib.call("qg_q8_0_pack_f16", w.qs.data_ptr(), w.d.data_ptr(), n_rows, k, out.codes.data_ptr(),
+              out.scales_t.data_ptr(), _stream_handle(stream))
+    return out
+
+
+def quantize_act_q8_0_f16(x: torch.Tensor, out: F16Codes | None = None, stream=None) -> F16Codes:
+    """f32 [rows, k] -> Q8_0 codes as binary16 and block-major f32 scales."""
+    _need(x, "x", torch.float32)
+    x2 = _as_2d(x)
+    rows, k = x2.shape
+    if out is None:
+        out = F16Codes.empty(rows, k, x.device)
+    out.check("out")
+    if (out.rows, out.k) != (rows, k):
+        raise ValueError("quantize_act_q8_0_f16: output of another shape")
+    _lib.call("quantize_act_q8_0_f16", x2.data_ptr(), rows, k, out.codes.data_ptr(), out.scales_t.data_ptr(),
+              _stream_handle(stream))
+    return out
+
+
+def qgemm_q8_0_prefill_tc2(w: F16Codes, x: F16Codes, y: torch.Tensor | None = None, tile_n: int = 0,
+                           stream=None) -> torch.Tensor:
+    """Wide-tile tensor-core prompt contraction; Y f32 [m, n_rows]."""
+    w.check("w")
+    x.check("x")
+    if x.k != w.k:
+        raise ValueError(f"qgemm_q8_0_prefill_tc2: activation width {x.k} != weight width {w.k}")
+    if y is None:
+        y = torch.empty((x.rows, w.rows), dtype=torch.float32, device=w.codes.device)
+    _need(y, "y", torch.float32, (x.rows, w.rows))
+    _lib.call("qgemm_q8_0_prefill_tc2", w.codes.data_ptr(), w.scales_t.data_ptr(), w.rows, w.k,
+              x.codes.data_ptr(), x.scales_t.data_ptr(), x.rows, y.data_ptr(), tile_n, _stream_handle(stream))
+    return y
+
+
 def qg_measure_mma_s8(iters: int, stream=None) -> int:
     """Launch the int8 mma.sync rate kernel (time the stream around it); returns
     the int-ops the launch performs."""

@@ -39,6 +39,10 @@ cudaError_t launch_quantize_act_tiles(const float *, int64_t, int64_t, void *, c
 bool prefill_tc_supported(int64_t k);
 bool prefill_bf16_supported(int64_t k);
 cudaError_t launch_mma_s8_rate(int64_t, int *, int64_t *, cudaStream_t);
+cudaError_t launch_pack_q8_0_f16(const int8_t *, const uint16_t *, int64_t, int64_t, uint16_t *, float *, cudaStream_t);
+cudaError_t launch_quantize_act_f16(const float *, int64_t, int64_t, uint16_t *, float *, cudaStream_t);
+cudaError_t launch_prefill_tc2(const uint16_t *, const float *, int64_t, int64_t, const uint16_t *, const float *,
+                               int64_t, float *, int, cudaStream_t);
 cudaError_t launch_prefill_bf16(const uint16_t *, int64_t, int64_t, const uint16_t *, int64_t, const uint16_t *, float,
                                 int, uint16_t *, float *, cudaStream_t);
 cudaError_t launch_prefill_tc(const int8_t *, const uint16_t *, int64_t, int64_t, const void *, int64_t, float *, int,
@@ -380,6 +384,61 @@ qg_status qgemm_bf16_prefill(const uint16_t *w, int64_t n_rows, int64_t k, const
                   overlap(xhat, xb, gamma, static_cast<size_t>(k) * 2)))
         return QG_ERR_SHAPE;
     return from_cuda(qg::launch_prefill_bf16(w, n_rows, k, x, m, gamma, eps, epilogue, xhat, y, stream));
+}
+
+int64_t qg_scales_ld(int64_t rows) { return rows < 0 ? -1 : (rows + 3) & ~int64_t(3); }
+
+qg_status qg_q8_0_pack_f16(const int8_t *w_qs, const uint16_t *w_d, int64_t n_rows, int64_t k, uint16_t *codes,
+                           float *scales_t, qg_stream_t stream)
+{
+    if (n_rows < 0 || n_rows > kMaxRows) return QG_ERR_SHAPE;
+    if (qg_status st = check_q8_k(k); st != QG_OK) return st;
+    if (n_rows == 0) return QG_OK;
+    if (!w_qs || !w_d || !codes || !scales_t) return QG_ERR_NULL;
+    if (!aligned(w_qs, 8) || !aligned(w_d, 2) || !aligned(codes, 16) || !aligned(scales_t, 4)) return QG_ERR_ALIGN;
+    const size_t nq = static_cast<size_t>(n_rows) * k, nd = static_cast<size_t>(n_rows) * (k / 32);
+    const size_t ns = static_cast<size_t>(qg_scales_ld(n_rows)) * (k / 32);
+    if (overlap(codes, nq * 2, w_qs, nq) || overlap(codes, nq * 2, w_d, nd * 2) || overlap(scales_t, ns * 4, w_qs, nq) ||
+        overlap(scales_t, ns * 4, w_d, nd * 2) || overlap(codes, nq * 2, scales_t, ns * 4))
+        return QG_ERR_SHAPE;
+    return from_cuda(qg::launch_pack_q8_0_f16(w_qs, w_d, n_rows, k, codes, scales_t, stream));
+}
+
+qg_status quantize_act_q8_0_f16(const float *x, int64_t rows, int64_t k, uint16_t *codes, float *scales_t,
+                                qg_stream_t stream)
+{
+    if (rows < 0 || rows > (int64_t(1) << 24)) return QG_ERR_SHAPE;
+    if (qg_status st = check_q8_k(k); st != QG_OK) return st;
+    if (rows == 0) return QG_OK;
+    if (!x || !codes || !scales_t) return QG_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(scales_t, 4)) return QG_ERR_ALIGN;
+    const size_t n = static_cast<size_t>(rows) * k, ns = static_cast<size_t>(qg_scales_ld(rows)) * (k / 32);
+    if (overlap(codes, n * 2, x, n * 4) || overlap(scales_t, ns * 4, x, n * 4) || overlap(codes, n * 2, scales_t, ns * 4))
+        return QG_ERR_SHAPE;
+    return from_cuda(qg::launch_quantize_act_f16(x, rows, k, codes, scales_t, stream));
+}
+
+qg_status qgemm_q8_0_prefill_tc2(const uint16_t *w_codes, const float *w_scales_t, int64_t n_rows, int64_t k,
+                                 const uint16_t *x_codes, const float *x_scales_t, int64_t m, float *y, int32_t tile_n,
+                                 qg_stream_t stream)
+{
+    if (n_rows < 0 || n_rows > kMaxRows || n_rows > INT32_MAX) return QG_ERR_SHAPE;
+    if (m < 0 || m > (int64_t(1) << 24)) return QG_ERR_SHAPE;
+    if (qg_status st = check_q8_k(k); st != QG_OK) return st;
+    if (tile_n != 0 && tile_n != 128 && tile_n != 192) return QG_ERR_UNSUPPORTED;
+    if (n_rows == 0 || m == 0) return QG_OK;
+    if (!w_codes || !w_scales_t || !x_codes || !x_scales_t || !y) return QG_ERR_NULL;
+    if (!aligned(w_codes, 16) || !aligned(w_scales_t, 16) || !aligned(x_codes, 16) || !aligned(x_scales_t, 16) ||
+        !aligned(y, 16))
+        return QG_ERR_ALIGN;
+    const size_t yb = static_cast<size_t>(m) * n_rows * 4;
+    if (overlap(y, yb, w_codes, static_cast<size_t>(n_rows) * k * 2) ||
+        overlap(y, yb, w_scales_t, static_cast<size_t>(qg_scales_ld(n_rows)) * (k / 32) * 4) ||
+        overlap(y, yb, x_codes, static_cast<size_t>(m) * k * 2) ||
+        overlap(y, yb, x_scales_t, static_cast<size_t>(qg_scales_ld(m)) * (k / 32) * 4))
+        return QG_ERR_SHAPE;
+    return from_cuda(
+        qg::launch_prefill_tc2(w_codes, w_scales_t, n_rows, k, x_codes, x_scales_t, m, y, tile_n, stream));
 }
 
 qg_status qg_measure_mma_s8(int64_t iters, int32_t *sink, int64_t *ops, qg_stream_t stream)

@@ -79,6 +79,18 @@ __device__ __forceinline__ void tmem_ld_16(uint32_t taddr, uint32_t *r)
           "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
+// 16 lanes x 32 columns in the 16x256b shape (no wait): for repeat r < 4 and
+// i < 4, out[4r + i] is lane base + t/4 + 8 (i / 2), column 8 r + 2 (t % 4) + i % 2,
+// t the thread's index in the warp; so out[4r], out[4r + 1] (and out[4r + 2],
+// out[4r + 3]) are two adjacent columns of one lane.
+__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t *r)
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
 // 8 consecutive 32-bit columns of this thread's TMEM lane (no wait).
 __device__ __forceinline__ void tmem_ld_8(uint32_t taddr, uint32_t *r)
 {
@@ -99,6 +111,18 @@ __device__ __forceinline__ void tmem_ld_32(uint32_t taddr, uint32_t *r)
         : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// The same wait, with the 32 registers of two earlier 16-register loads passed
+// through it, so that no use of them can be scheduled before it.
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t *a, uint32_t *b)
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]),
+                   "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15]),
+                   "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7]),
+                   "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]), "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15])
+                 :
+                 : "memory");
+}
 
 __device__ __forceinline__ uint64_t pack2(float lo, float hi)
 {

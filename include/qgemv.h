@@ -359,6 +359,43 @@ QG_API qg_status qg_debug_block_dots_q8_0(const int8_t *w_qs, int64_t n_rows, in
                                    qg_stream_t stream);
 
 /*
+ * Operands for qgemm_q8_0_prefill_tc2, the prompt contraction over wide tiles
+ * ([Phobos] Fast Decode: prompt processing on the tensor cores; GPU Performance
+ * Heisenbugs: exact integer values on the tensor cores).  Codes are held as
+ * binary16 values (exact: integers in [-127, 127]) in plain row-major matrices,
+ * scales as f32 block-major [k/32][ld] with ld = qg_scales_ld(rows), rows rounded
+ * up to a multiple of four so that each block's row starts on 16 bytes (the
+ * padding entries are neither written nor read).
+ *
+ * qg_q8_0_pack_f16 - weight planes -> that form (a one-time load step).
+ *   w_qs: device int8 [n_rows][k] (read), 8-byte aligned; w_d: binary16 bits
+ *   [n_rows][k/32] (read); codes: device binary16 [n_rows][k] (written),
+ *   16-byte aligned; scales_t: device f32 [k/32][ld] (written).  k a
+ *   multiple of 32.  Outputs must not overlap inputs (QG_ERR_SHAPE).
+ *
+ * quantize_act_q8_0_f16 - quantize_act_q8_0 (same codes, same binary16-rounded
+ *   scales) writing that form: x f32 [rows][k] (read, 16-byte aligned),
+ *   codes binary16 [rows][k], scales_t f32 [k/32][ld] (written).
+ *
+ * qgemm_q8_0_prefill_tc2 - Y[m][n] = sum_j f32(d_x[m][j]) f32(d_w[n][j]) S_j[m][n]
+ *   on tcgen05 over 128 x tile_n output tiles (tile_n 128 or 192, or 0 to let
+ *   the library choose): exact block sums S_j in TMEM, the rescale in f32
+ *   registers.  w_codes, w_scales_t: from qg_q8_0_pack_f16; x_codes, x_scales_t:
+ *   from quantize_act_q8_0_f16 for m rows; y: device f32 [m][n_rows] (written).
+ *   Operands 16-byte aligned, k a multiple of 32, m <= 2^24; y must not overlap
+ *   the operands (QG_ERR_SHAPE).  Runs one CTA per SM; if an operand copy stalls
+ *   beyond one second the kernel writes NaN for the tiles it has left.
+ */
+QG_API int64_t qg_scales_ld(int64_t rows);
+QG_API qg_status qg_q8_0_pack_f16(const int8_t *w_qs, const uint16_t *w_d, int64_t n_rows, int64_t k,
+                                  uint16_t *codes, float *scales_t, qg_stream_t stream);
+QG_API qg_status quantize_act_q8_0_f16(const float *x, int64_t rows, int64_t k, uint16_t *codes,
+                                       float *scales_t, qg_stream_t stream);
+QG_API qg_status qgemm_q8_0_prefill_tc2(const uint16_t *w_codes, const float *w_scales_t, int64_t n_rows,
+                                        int64_t k, const uint16_t *x_codes, const float *x_scales_t,
+                                        int64_t m, float *y, int32_t tile_n, qg_stream_t stream);
+
+/*
  * qg_measure_mma_s8 - times nothing itself: launches a grid (4 CTAs per SM) whose
  * warps issue `iters` rounds of eight independent mma.sync.m16n8k32 s8 MMAs on
  * register operands, the int8 tensor path that sm_103a offers ([Phobos] GPU

@@ -130,6 +130,34 @@ def test_prefill_tc_argument_errors(lib):
     assert tc(None, FAKE, 8, 256, FAKE, 1, FAKE, 0, None) == 1
 
 
+def test_prefill_tc2_argument_errors(lib):
+    assert lib.qg_scales_ld(0) == 0 and lib.qg_scales_ld(1) == 4 and lib.qg_scales_ld(512) == 512
+    assert lib.qg_scales_ld(7169) == 7172 and lib.qg_scales_ld(-1) == -1
+    g = 1 << 28  # operands placed far apart so that only the checked property fails
+    W, WS, X, XS, Y = FAKE, FAKE + g, FAKE + 2 * g, FAKE + 3 * g, FAKE + 4 * g
+    tc2 = lib.qgemm_q8_0_prefill_tc2
+    assert tc2(W, WS, 64, 48, X, XS, 5, Y, 0, None) == 3           # k a multiple of 32
+    assert tc2(W, WS, 64, 256, X, XS, (1 << 24) + 1, Y, 0, None) == 3
+    assert tc2(W, WS, 64, 256, X, XS, 5, Y, 64, None) == 4         # tile widths 0, 128, 192
+    assert tc2(W, WS, 64, 256, X, XS, 5, Y + 8, 0, None) == 2
+    assert tc2(W, WS + 4, 64, 256, X, XS, 5, Y, 0, None) == 2
+    assert tc2(W, WS, 64, 256, X, None, 5, Y, 0, None) == 1
+    assert tc2(W, WS, 64, 256, X, XS, 5, X + 64, 0, None) == 3     # y over the activation codes
+    assert tc2(None, None, 64, 256, None, None, 0, None, 0, None) == 0
+    pk = lib.qg_q8_0_pack_f16
+    assert pk(W, WS, 8, 40, X, XS, None) == 3
+    assert pk(W + 4, WS, 8, 64, X, XS, None) == 2
+    assert pk(W, WS, 8, 64, X + 8, XS, None) == 2
+    assert pk(W, WS, 8, 64, None, XS, None) == 1
+    assert pk(W, WS, 8, 64, W + 64, XS, None) == 3                 # codes over the int8 plane
+    qa = lib.quantize_act_q8_0_f16
+    assert qa(X, 3, 33, W, WS, None) == 3
+    assert qa(X + 4, 3, 64, W, WS, None) == 2
+    assert qa(X, 3, 64, W, None, None) == 1
+    assert qa(X, 3, 64, X + 128, WS, None) == 3
+    assert qa(None, 0, 64, None, None, None) == 0
+
+
 def test_act_tiles_size_and_errors(lib):
     # one record of 8192 code bytes + 256 scale bytes per (128-row tile, block)
     assert lib.qg_act_tiles_bytes(130, 256) == 2 * 8 * 8448

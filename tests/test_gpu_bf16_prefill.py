@@ -211,6 +211,85 @@ def test_prefill_tc_matches_mma_sync_path(torch, orc):
 
 
 # ---------------------------------------------------------------------------
+# Q8_0 prompt contraction over wide tiles (binary16 codes, block-major scales)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n,k", [(37, 64), (70, 96), (7168, 1024), (1, 32)])
+def test_pack_f16_bit_exact(torch, n, k):
+    from block_quantized_decode_rmsnorm_gb300 import api
+
+    qs, d = synth.q8_0_weight_planes(5 * n + k, 10, n, k)
+    p = api.qg_q8_0_pack_f16(weight(qs, d))
+    torch.cuda.synchronize()
+    codes, sc = p.codes.cpu().numpy(), p.scales_t.cpu().numpy()
+    assert sc.shape == (k // 32, (n + 3) // 4 * 4)
+    assert np.array_equal(codes.astype(np.float32), qs.astype(np.float32))
+    assert np.array_equal(sc[:, :n].T, d.view(np.float16).astype(np.float32))
+
+
+@pytest.mark.parametrize("rows,k", [(37, 1024), (128, 256), (129, 96), (1, 32), (512, 1024)])
+def test_quantize_act_f16_bit_exact(torch, orc, rows, k):
+    from block_quantized_decode_rmsnorm_gb300 import api
+
+    x = synth.f32_normal(41 + rows, 0, (rows, k))
+    x[min(3, rows - 1), :32] = 0.0
+    x[rows // 2, 32 * (k // 64):32 * (k // 64) + 32] *= 1e-30  # subnormal-range block
+    xc = api.quantize_act_q8_0_f16(to_dev(x, torch))
+    torch.cuda.synchronize()
+    qo, do = orc.quantize_q8_0(x)
+    assert np.array_equal(xc.codes.cpu().numpy().astype(np.float32), qo.astype(np.float32))
+    assert np.array_equal(xc.scales_t.cpu().numpy()[:, :rows].T, do.view(np.float16).astype(np.float32))
+
+
+@pytest.mark.parametrize("m,n,k,tile_n", [
+    (1, 64, 256, 0), (5, 70, 96, 128), (5, 70, 96, 192),   # K = 96: the last step holds one block
+    (4, 129, 256, 192), (130, 200, 1024, 192), (37, 129, 4096, 0),
+    (3, 40, 8192, 128),                                   # many K steps
+    (600, 4000, 256, 128),                                # 160 tiles: more than one per CTA
+    (512, 7168, 1024, 0), (512, 7168, 1024, 128), (512, 7168, 1024, 192),
+])
+def test_prefill_tc2(torch, orc, m, n, k, tile_n):
+    from block_quantized_decode_rmsnorm_gb300 import api
+
+    qs, d = synth.q8_0_weight_planes(m + 3 * n + 1, 10, n, k)
+    x = synth.f32_normal(m + k + 2, 0, (m, k))
+    w2 = api.qg_q8_0_pack_f16(weight(qs, d))
+    x2 = api.quantize_act_q8_0_f16(to_dev(x, torch))
+    gy = Guarded(torch, (m, n), torch.float32)
+    api.qgemm_q8_0_prefill_tc2(w2, x2, y=gy.view, tile_n=tile_n)
+    torch.cuda.synchronize()
+    gy.check()
+    y = gy.view.cpu().numpy()
+    xq, xdo = orc.quantize_q8_0(x)
+    rows = np.arange(m) if m <= 300 else np.unique(np.concatenate([np.arange(0, m, 37), [m - 1, 127, 128]]))
+    y64, a64 = orc.gemv_q8_0(qs, d, xq[rows], xdo[rows])
+    assert_close(y[rows], y64, a64, TOL_Q8, f"prefill tc2 {m}x{n}x{k} tile {tile_n}")
+    assert not np.isnan(y).any()
+
+
+def test_prefill_tc2_matches_tc_and_is_deterministic(torch, orc):
+    """The wide-tile kernel and the tile-record kernel agree within the combined
+    tolerance on the same operands; both tile widths give identical bits (the
+    per-element order of operations does not depend on the tile)."""
+    from block_quantized_decode_rmsnorm_gb300 import api
+
+    m, n, k = 200, 384, 2048
+    qs, d = synth.q8_0_weight_planes(91, 10, n, k)
+    x = synth.f32_normal(92, 0, (m, k))
+    xd_ = to_dev(x, torch)
+    w = weight(qs, d)
+    w2, x2 = api.qg_q8_0_pack_f16(w), api.quantize_act_q8_0_f16(xd_)
+    y1 = api.qgemm_q8_0_prefill_tc2(w2, x2, tile_n=128).cpu().numpy()
+    y2 = api.qgemm_q8_0_prefill_tc2(w2, x2, tile_n=192).cpu().numpy()
+    y3 = api.qgemm_q8_0_prefill_tc2(w2, x2, tile_n=192).cpu().numpy()
+    assert np.array_equal(y1, y2) and np.array_equal(y2, y3)
+    yt = api.qgemm_q8_0_prefill_tc(w, api.quantize_act_q8_0_tiles(xd_)).cpu().numpy()
+    xq, xdo = orc.quantize_q8_0(x)
+    _, a64 = orc.gemv_q8_0(qs, d, xq, xdo)
+    assert_close(y1, yt, a64, 2 * TOL_Q8, "tc2 vs tc")
+
+
+# ---------------------------------------------------------------------------
 # bf16 projection for a whole prompt on the tensor cores
 # ---------------------------------------------------------------------------
 
