@@ -289,6 +289,33 @@ def test_prefill_tc2_matches_tc_and_is_deterministic(torch, orc):
     assert_close(y1, yt, a64, 2 * TOL_Q8, "tc2 vs tc")
 
 
+def test_prefill_tc2_graph_replay(torch):
+    """Quantize + wide-tile contraction captured in a CUDA graph: replays give the
+    eager call's bits (the library allocates nothing and takes the stream)."""
+    from block_quantized_decode_rmsnorm_gb300 import api
+
+    m, n, k = 130, 400, 512
+    qs, d = synth.q8_0_weight_planes(93, 10, n, k)
+    w2 = api.qg_q8_0_pack_f16(weight(qs, d))
+    x = to_dev(synth.f32_normal(94, 0, (m, k)), torch)
+    x2 = api.F16Codes.empty(m, k, "cuda")
+    y = torch.empty((m, n), dtype=torch.float32, device="cuda")
+    api.quantize_act_q8_0_f16(x, out=x2)
+    ref = api.qgemm_q8_0_prefill_tc2(w2, x2).cpu().numpy()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            api.quantize_act_q8_0_f16(x, out=x2, stream=s)
+            api.qgemm_q8_0_prefill_tc2(w2, x2, y=y, stream=s)
+    for _ in range(2):
+        y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(y.cpu().numpy(), ref)
+
+
 # ---------------------------------------------------------------------------
 # bf16 projection for a whole prompt on the tensor cores
 # ---------------------------------------------------------------------------
