@@ -11,7 +11,7 @@ _API_NAMES = {
     "qgemm_q8_0_prefill", "qg_debug_block_dots_q8_0", "decode_ffn_q8_0", "qg_ffn_up_q8_0",
     "qg_decode_ffn_q8_0", "qg_decode_layer_q8_0", "qg_decode_layer_partials", "qg_decode_layer_finish", "LayerStack", "qg_decode_layers_q8_0_noalloc", "qg_q8_0_column_blocks", "prepare_one_launch", "quantize_act_q8_0_tiles", "qgemm_q8_0_prefill_tc", "ActTiles", "Q8Weight", "FFNLayer",
     "FFNBuffers", "q8_weight_from_numpy", "bf16_from_bits", "qgemm_bf16_prefill", "qg_measure_mma_s8",
-    "qg_q8_0_pack_f16", "quantize_act_q8_0_f16", "qgemm_q8_0_prefill_tc2", "F16Codes",
+    "qg_q8_0_pack_f16", "quantize_act_q8_0_f16", "qg_decode_ffn_q8_0_out", "qgemm_q8_0_prefill_tc2", "F16Codes",
 }
 
 

@@ -460,6 +460,33 @@ def qg_decode_ffn_q8_0(x: torch.Tensor, layer: FFNLayer, buf: FFNBuffers, eps: f
               layer.down.d.data_ptr(), buf.h.data_ptr(), buf.hq.data_ptr(), buf.hd.data_ptr(), _stream_handle(stream))
 
 
+def _need_reachable(t: torch.Tensor, name: str, shape) -> None:
+    """f32 contiguous tensor on a CUDA device or in pinned host memory (which the
+    kernels reach directly through unified addressing)."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not (t.is_cuda or (t.device.type == "cpu" and t.is_pinned())):
+        raise ValueError(f"{name} must be on a CUDA device or in pinned host memory")
+    if t.dtype != torch.float32 or not t.is_contiguous() or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must be contiguous float32 of shape {tuple(shape)}")
+
+
+def qg_decode_ffn_q8_0_out(x_in: torch.Tensor, x_out: torch.Tensor, layer: FFNLayer, buf: FFNBuffers,
+                           eps: float = 1e-6, stream=None) -> None:
+    """x_out <- x_in + down(SiLU(g)*u) in two launches; x_in / x_out may be pinned
+    host tensors (the first layer of a step reading the host input, the last one
+    writing the host result)."""
+    hidden = layer.gamma.shape[-1]
+    ffn = layer.down.k
+    if x_in.numel() != hidden:
+        raise ValueError(f"x_in must hold {hidden} values")
+    _need_reachable(x_in, "x_in", x_in.shape)
+    _need_reachable(x_out, "x_out", x_in.shape)
+    _lib.call("qg_decode_ffn_q8_0_out", x_in.data_ptr(), x_out.data_ptr(), layer.gamma.data_ptr(), hidden, ffn,
+              float(eps), layer.gate_up.qs.data_ptr(), layer.gate_up.d.data_ptr(), layer.down.qs.data_ptr(),
+              layer.down.d.data_ptr(), buf.h.data_ptr(), buf.hq.data_ptr(), buf.hd.data_ptr(), _stream_handle(stream))
+
+
 def qg_q8_0_column_blocks(w: Q8Weight, stream=None) -> Q8Weight:
     """Row-major planes -> column-block planes: values [k/32, n, 32], scales [k/32, n]
     (returned as a Q8Weight whose tensors have those shapes)."""

@@ -257,25 +257,38 @@ qg_status qg_ffn_up_q8_0(const float *x, const float *gamma, int64_t hidden, flo
                                        stream));
 }
 
-qg_status qg_decode_ffn_q8_0(float *x, const float *gamma, int64_t hidden, int64_t ffn, float eps,
-                             const int8_t *wgu_qs, const uint16_t *wgu_d, const int8_t *wdn_qs,
-                             const uint16_t *wdn_d, float *h, int8_t *hq, uint16_t *hd, qg_stream_t stream)
+qg_status qg_decode_ffn_q8_0_out(const float *x_in, float *x_out, const float *gamma, int64_t hidden, int64_t ffn,
+                                 float eps, const int8_t *wgu_qs, const uint16_t *wgu_d, const int8_t *wdn_qs,
+                                 const uint16_t *wdn_d, float *h, int8_t *hq, uint16_t *hd, qg_stream_t stream)
 {
     if (hidden <= 0 || hidden % 32 != 0 || ffn <= 0 || ffn % 32 != 0 || ffn > kMaxRows / 2 || ffn > kMaxK)
         return QG_ERR_SHAPE;
     if (!(eps >= 0.0f)) return QG_ERR_SHAPE;
     if (!qg::ffn_up_supported(hidden, ffn)) return QG_ERR_UNSUPPORTED;
-    if (!x || !gamma || !wgu_qs || !wgu_d || !wdn_qs || !wdn_d || !h || !hq || !hd) return QG_ERR_NULL;
-    if (!aligned(x, 16) || !aligned(gamma, 16) || !aligned(wgu_qs, 32) || !aligned(wgu_d, 16) ||
-        !aligned(wdn_qs, 32) || !aligned(wdn_d, 16) || !aligned(h, 16) || !aligned(hq, 32) || !aligned(hd, 2))
+    if (!x_in || !x_out || !gamma || !wgu_qs || !wgu_d || !wdn_qs || !wdn_d || !h || !hq || !hd) return QG_ERR_NULL;
+    if (!aligned(x_in, 16) || !aligned(x_out, 16) || !aligned(gamma, 16) || !aligned(wgu_qs, 32) ||
+        !aligned(wgu_d, 16) || !aligned(wdn_qs, 32) || !aligned(wdn_d, 16) || !aligned(h, 16) || !aligned(hq, 32) ||
+        !aligned(hd, 2))
         return QG_ERR_ALIGN;
-    qg_status st = from_cuda(qg::launch_ffn_up(x, gamma, hidden, eps, wgu_qs, wgu_d, ffn, h, hq, hd, nullptr,
+    // in place, or apart: a partial overlap would let the down projection read
+    // residual rows that another CTA has already overwritten
+    const size_t xb = static_cast<size_t>(hidden) * sizeof(float);
+    if (x_in != x_out && overlap(x_in, xb, x_out, xb)) return QG_ERR_SHAPE;
+    qg_status st = from_cuda(qg::launch_ffn_up(x_in, gamma, hidden, eps, wgu_qs, wgu_d, ffn, h, hq, hd, nullptr,
                                                nullptr, nullptr, stream));
     if (st != QG_OK) return st;
     if (qg::prefetch_supported(hidden, ffn) && aligned(wdn_d, 16))
-        return from_cuda(qg::launch_gemv_prefetch(wdn_qs, wdn_d, hidden, ffn, hq, hd, QG_EPI_RESIDUAL_ADD, x, x,
-                                                  stream));
-    return from_cuda(qg::launch_gemv_q8_0(wdn_qs, wdn_d, hidden, ffn, hq, hd, 1, QG_EPI_RESIDUAL_ADD, x, x, stream));
+        return from_cuda(qg::launch_gemv_prefetch(wdn_qs, wdn_d, hidden, ffn, hq, hd, QG_EPI_RESIDUAL_ADD, x_in,
+                                                  x_out, stream));
+    return from_cuda(
+        qg::launch_gemv_q8_0(wdn_qs, wdn_d, hidden, ffn, hq, hd, 1, QG_EPI_RESIDUAL_ADD, x_in, x_out, stream));
+}
+
+qg_status qg_decode_ffn_q8_0(float *x, const float *gamma, int64_t hidden, int64_t ffn, float eps,
+                             const int8_t *wgu_qs, const uint16_t *wgu_d, const int8_t *wdn_qs,
+                             const uint16_t *wdn_d, float *h, int8_t *hq, uint16_t *hd, qg_stream_t stream)
+{
+    return qg_decode_ffn_q8_0_out(x, x, gamma, hidden, ffn, eps, wgu_qs, wgu_d, wdn_qs, wdn_d, h, hq, hd, stream);
 }
 
 static bool layer_shape_ok(int64_t hidden, int64_t ffn)

@@ -244,6 +244,20 @@ QG_API qg_status qg_decode_ffn_q8_0(float *x, const float *gamma, int64_t hidden
                                     int8_t *hq, uint16_t *hd, qg_stream_t stream);
 
 /*
+ * qg_decode_ffn_q8_0_out - the same block out of place: x_out = x_in + down(h),
+ * h computed from x_in.  x_in and x_out are the same pointer (in place, as
+ * qg_decode_ffn_q8_0) or do not overlap (QG_ERR_SHAPE otherwise); both are f32
+ * [hidden], 16-byte aligned, and may be device memory or pinned host memory
+ * (read or written by the kernels directly over the host link), so a step can
+ * take its input from, and leave its result in, host buffers without separate
+ * copies.  Other arguments and errors as qg_decode_ffn_q8_0.
+ */
+QG_API qg_status qg_decode_ffn_q8_0_out(const float *x_in, float *x_out, const float *gamma, int64_t hidden,
+                                        int64_t ffn, float eps, const int8_t *wgu_qs, const uint16_t *wgu_d,
+                                        const int8_t *wdn_qs, const uint16_t *wdn_d, float *h, int8_t *hq,
+                                        uint16_t *hd, qg_stream_t stream);
+
+/*
  * qg_decode_layer_q8_0 - one decode feed-forward block in ONE launch, its
  * input and output each held unreduced as a base vector plus partial vectors:
  *   x      = r_in + p_in[0] + ... + p_in[n_in - 1]        (f32, in that order)

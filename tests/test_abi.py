@@ -117,6 +117,22 @@ def test_fused_ffn_argument_errors(lib):
     assert d(FAKE, FAKE, 1024, 0, eps, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == 3
 
 
+def test_decode_ffn_out_argument_errors(lib):
+    f = lib.qg_decode_ffn_q8_0_out
+    eps = ctypes.c_float(1e-6)
+    g = 1 << 20
+    XI, XO = FAKE, FAKE + 8 * g
+    args = lambda xi, xo, hidden=1024: (xi, xo, FAKE + 2 * g, hidden, 3584, eps, FAKE + 3 * g, FAKE + 4 * g,
+                                        FAKE + 5 * g, FAKE + 6 * g, FAKE + 7 * g, FAKE + 9 * g, FAKE + 10 * g, None)
+    # partial overlap of input and output (in place, xi == xo, is allowed)
+    assert f(*args(XI, XI + 64)) == 3
+    assert f(*args(XI + 4, XO)) == 2
+    assert f(*args(XI, XO + 8)) == 2
+    assert f(*args(None, XO)) == 1
+    assert f(*args(XI, None)) == 1
+    assert f(*args(XI, XO, 992)) == 4
+
+
 def test_prefill_tc_argument_errors(lib):
     tc = lib.qgemm_q8_0_prefill_tc
     # K must be a multiple of 256 for the tensor-core path

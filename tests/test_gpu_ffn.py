@@ -209,6 +209,61 @@ def test_fused_graph_replay(torch, orc):
     assert not np.array_equal(want, eager)
 
 
+def test_decode_ffn_out_of_place_host_buffers(torch, orc):
+    """The out-of-place layer with its input read from, and its result written to,
+    pinned host memory gives the in-place device result bit for bit, eagerly and
+    replayed from a graph (the end-to-end step of the benchmark)."""
+    from block_quantized_decode_rmsnorm_gb300 import api
+
+    n_layers = 3
+    cases = [synth.ffn_case(7, layer=l) for l in range(n_layers)]
+    layers = [_layer(torch, c) for c in cases]
+    buf = api.FFNBuffers.allocate(HIDDEN, FFN, "cuda")
+    x0 = cases[0]["x"]
+    ref = to_dev(x0, torch)
+    api.qg_decode_ffn_q8_0(ref, layers[0], buf, EPS)
+    torch.cuda.synchronize()
+    one = ref.cpu().numpy()
+    for l in layers[1:]:
+        api.qg_decode_ffn_q8_0(ref, l, buf, EPS)
+    torch.cuda.synchronize()
+    want = ref.cpu().numpy()
+
+    x_host = torch.from_numpy(x0.copy()).pin_memory()
+    out_host = torch.zeros_like(x_host).pin_memory()
+    api.qg_decode_ffn_q8_0_out(x_host, out_host, layers[0], buf, EPS)  # host to host, one layer
+    torch.cuda.synchronize()
+    assert np.array_equal(out_host.numpy(), one)
+    assert np.array_equal(x_host.numpy(), x0)  # the input is left as it was
+
+    x = torch.empty(x0.shape, dtype=torch.float32, device="cuda")
+
+    def step(stream=None):
+        api.qg_decode_ffn_q8_0_out(x_host, x, layers[0], buf, EPS, stream=stream)
+        for l in layers[1:-1]:
+            api.qg_decode_ffn_q8_0(x, l, buf, EPS, stream=stream)
+        api.qg_decode_ffn_q8_0_out(x, out_host, layers[-1], buf, EPS, stream=stream)
+
+    out_host.zero_()
+    step()
+    torch.cuda.synchronize()
+    assert np.array_equal(out_host.numpy(), want)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            step(stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        out_host.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(out_host.numpy(), want)
+    with pytest.raises(ValueError):
+        api.qg_decode_ffn_q8_0_out(torch.from_numpy(x0.copy()), x, layers[0], buf, EPS)  # pageable host memory
+
+
 @pytest.mark.parametrize("hidden,ffn", [(256, 96), (2048, 1024), (768, 64)])
 def test_fused_other_shapes(torch, orc, hidden, ffn):
     from block_quantized_decode_rmsnorm_gb300 import api
