@@ -7,7 +7,8 @@
 //
 // GB300 mapping.  Codes are held as binary16 values (exact: integers in
 // [-127, 127]) in plain row-major matrices, weights packed once at load time and
-// activations by their quantize kernel, scales as f32 block-major [k/32][rows].
+// activations by their quantize kernel, scales as f32 block-major [k/32][ld]
+// (ld = rows rounded up to four, so that every block row starts on 16 bytes).
 // The contraction is the TMA -> MMA -> TMEM pipeline of the bf16 prompt kernel
 // with the per-block rescale the Q8_0 format needs:
 //  * one thread copies per K step of 64 codes (two blocks) a 128 x 64 activation
@@ -97,7 +98,7 @@ __global__ void quantize_act_f16_kernel(const float *x, int64_t m, int k, uint16
 constexpr int T2_BM = 128;
 constexpr int T2_BK = 64;  // codes per K step: two blocks, one 128-byte swizzle row of binary16
 constexpr int T2_CW = 64;              // tile columns per epilogue warp
-constexpr int T2_XPOSE = 32 * 40 * 4;  // per epilogue warp: a padded 32 x 32 f32 block
+constexpr int T2_XPOSE = 32 * 40 * 4;  // per epilogue warp: a 32 x 32 f32 block in rows of 40 floats
 
 template <int BN>
 struct T2Layout {
