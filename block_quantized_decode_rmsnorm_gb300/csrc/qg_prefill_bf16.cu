@@ -120,13 +120,6 @@ __global__ void __launch_bounds__(NR_THREADS) rmsnorm_bf16_rows_kernel(const uin
     }
 }
 
-// silu(g) * u = g u / (1 + e^-g) with the fast exponential and division (a few
-// ulp; for g below about -88, e^-g is infinite and the quotient is 0).
-__device__ __forceinline__ float silu_mul_fast(float g, float u)
-{
-    return __fdividef(g, 1.0f + __expf(-g)) * u;
-}
-
 // ---------------------------------------------------------------------------
 // the projection
 // ---------------------------------------------------------------------------
@@ -260,7 +253,7 @@ __global__ void __launch_bounds__(PB_THREADS, 1)
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
                     v[j] = !ok ? __int_as_float(0x7fc00000)
-                               : p.silu ? silu_mul_fast(__uint_as_float(a[j]), __uint_as_float(b[j])) : __uint_as_float(a[j]);
+                               : p.silu ? silu_mul(__uint_as_float(a[j]), __uint_as_float(b[j])) : __uint_as_float(a[j]);
                 // lane l holds row l of the block: through shared memory (row
                 // stride 33 floats, conflict-free both ways), then lane l stores
                 // column l of each row
