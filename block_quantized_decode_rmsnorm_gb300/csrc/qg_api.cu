@@ -1,5 +1,6 @@
 // extern "C" entry points of libqgemv.so: argument checks, then one launch.
 // Declarations and the full contract are in include/qgemv.h.
+#include <map>
 #include <mutex>
 
 #include "qg_common.cuh"
@@ -64,6 +65,22 @@ int num_sms()
         cache[dev] = n;
     }
     return cache[dev];
+}
+
+cudaError_t opt_in_smem(const void *func, int bytes)
+{
+    static std::mutex mu;
+    static std::map<std::pair<int, const void *>, int> done;  // (device, kernel) -> bytes opted in
+    int dev = 0;
+    if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    int &have = done[{dev, func}];
+    if (have >= bytes) return cudaSuccess;
+    if (cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        e != cudaSuccess)
+        return e;
+    have = bytes;
+    return cudaSuccess;
 }
 
 }  // namespace qg

@@ -328,6 +328,10 @@ constexpr uint64_t kCopyWaitLimitNs = 1000000000ull;
 // ---------------------------------------------------------------------------
 namespace qg {
 int num_sms();
+// Opt `func` in to `bytes` of dynamic shared memory on the current device.  The
+// opt-in is an attribute of the kernel in each device's context, so it is made
+// once per (device, kernel), and again only when a larger size is asked for.
+cudaError_t opt_in_smem(const void *func, int bytes);
 // Launch with programmatic stream serialization enabled.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,

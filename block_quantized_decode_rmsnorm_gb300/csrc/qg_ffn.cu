@@ -43,7 +43,6 @@
 //    forms x = r + sum of the partials in a fixed order while it loads its
 //    input anyway, so no float atomics and no extra pass are needed and the
 //    result is the same on every run.
-#include <mutex>
 
 #include "qg_common.cuh"
 #include "qg_norm.cuh"
@@ -553,13 +552,7 @@ bool decode_layer_supported(int64_t k, int64_t half)
 template <int NBL, bool DOWN>
 static cudaError_t ffn_up_attr()
 {
-    static std::once_flag once;
-    static cudaError_t err = cudaSuccess;
-    std::call_once(once, [] {
-        err = cudaFuncSetAttribute(ffn_up_kernel<NBL, DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   static_cast<int>(kMaxSmem));
-    });
-    return err;
+    return opt_in_smem(reinterpret_cast<const void *>(ffn_up_kernel<NBL, DOWN>), static_cast<int>(kMaxSmem));
 }
 
 static FfnUpParams ffn_up_params(const float *x, const float *gamma, int64_t k, float eps, const int8_t *w_qs,
@@ -647,13 +640,7 @@ bool prefetch_supported(int64_t n_rows, int64_t k)
 template <int NBL>
 static cudaError_t prefetch_attr()
 {
-    static std::once_flag once;
-    static cudaError_t err = cudaSuccess;
-    std::call_once(once, [] {
-        err = cudaFuncSetAttribute(gemv_prefetch_kernel<NBL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   static_cast<int>(kMaxSmem));
-    });
-    return err;
+    return opt_in_smem(reinterpret_cast<const void *>(gemv_prefetch_kernel<NBL>), static_cast<int>(kMaxSmem));
 }
 
 template <int NBL>

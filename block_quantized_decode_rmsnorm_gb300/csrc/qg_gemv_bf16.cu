@@ -200,12 +200,7 @@ static cudaError_t launch_bf16_nch(const Bf16Params &p, cudaStream_t s)
 {
     auto kernel = gemv_bf16_kernel<R, NCH>;
     const size_t smem = (static_cast<size_t>(p.n_groups) * 8 + 2 * (BF16_THREADS / 32) + 1) * sizeof(float);
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [&] {
-        attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
+    if (cudaError_t e = opt_in_smem(reinterpret_cast<const void *>(kernel), 200 * 1024); e != cudaSuccess) return e;
     // occupancy depends on the shared-memory size, i.e. on k: cache the last answer
     static std::mutex mu;
     static size_t occ_smem = 0;

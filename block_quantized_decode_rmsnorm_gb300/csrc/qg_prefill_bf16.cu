@@ -30,7 +30,6 @@
 // Every barrier wait is bounded by the global timer; a stalled pipeline aborts
 // (NaN outputs for the tiles left) instead of hanging.
 #include <cuda.h>
-#include <mutex>
 
 #include "qg_common.cuh"
 #include "qg_norm.cuh"
@@ -330,12 +329,8 @@ cudaError_t launch_prefill_bf16(const uint16_t *w, int64_t n_rows, int64_t k, co
     p.n_per_tile = p.silu ? 128 : PB_BN;
     p.m_tiles = (m + PB_BM - 1) / PB_BM;
     p.tiles = p.m_tiles * ((p.n_out + p.n_per_tile - 1) / p.n_per_tile);
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(prefill_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PB_SMEM);
-    });
-    if (attr != cudaSuccess) return attr;
+    if (cudaError_t e = opt_in_smem(reinterpret_cast<const void *>(prefill_bf16_kernel), PB_SMEM); e != cudaSuccess)
+        return e;
     const int64_t grid = p.tiles < num_sms() ? p.tiles : num_sms();
     return launch_pdl(prefill_bf16_kernel, dim3(static_cast<unsigned>(grid)), dim3(PB_THREADS), PB_SMEM, s, amap,
                       bmap, p);

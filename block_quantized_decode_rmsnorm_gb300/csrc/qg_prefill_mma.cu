@@ -12,7 +12,6 @@
 // 32 x 32, cp.async multi-stage staging of the int8 tiles (16-byte chunks,
 // XOR-swizzled so ldmatrix reads are conflict-free), all scales of the CTA's
 // rows staged once as f32.
-#include <mutex>
 
 #include "qg_common.cuh"
 
@@ -237,14 +236,11 @@ cudaError_t launch_prefill_mma(const int8_t *w_qs, const uint16_t *w_d, int64_t 
     if (p.nb > PF_MAX_NB) return cudaErrorInvalidValue;
     const size_t smem =
         PF_STAGES * (PF_BM + PF_BN) * 32 + static_cast<size_t>(PF_BM + PF_BN) * (p.nb + 1) * sizeof(float);
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(prefill_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(PF_STAGES * (PF_BM + PF_BN) * 32 +
-                                                         (PF_BM + PF_BN) * (PF_MAX_NB + 1) * sizeof(float)));
-    });
-    if (attr_err != cudaSuccess) return attr_err;
+    if (cudaError_t e = opt_in_smem(reinterpret_cast<const void *>(prefill_mma_kernel),
+                                    static_cast<int>(PF_STAGES * (PF_BM + PF_BN) * 32 +
+                                                     (PF_BM + PF_BN) * (PF_MAX_NB + 1) * sizeof(float)));
+        e != cudaSuccess)
+        return e;
     const dim3 grid(static_cast<unsigned>((n_rows + PF_BN - 1) / PF_BN), static_cast<unsigned>((m + PF_BM - 1) / PF_BM));
     return launch_pdl(prefill_mma_kernel, grid, dim3(PF_THREADS), smem, s, p);
 }

@@ -41,7 +41,6 @@
 // and a stalled pipeline aborts (NaN outputs for the tiles left) instead of
 // hanging.
 #include <cuda.h>
-#include <mutex>
 
 #include "qg_common.cuh"
 #include "qg_tc.cuh"
@@ -459,13 +458,10 @@ static cudaError_t launch_prefill_tc_bn(EncodeTiledFn enc, const int8_t *w_qs, c
     p.m_tiles = act_tiles(m);
     p.tiles = p.m_tiles * ((n_rows + BN - 1) / BN);
     const size_t smem = L::BYTES + 1024;  // + alignment of the base to 1024 bytes
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(prefill_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaError_t e = opt_in_smem(reinterpret_cast<const void *>(prefill_tc_kernel<BN>),
                                     static_cast<int>(TcLayout<BN>::BYTES + 1024));
-    });
-    if (attr != cudaSuccess) return attr;
+        e != cudaSuccess)
+        return e;
     const int64_t grid = p.tiles < num_sms() ? p.tiles : num_sms();
     return launch_pdl(prefill_tc_kernel<BN>, dim3(static_cast<unsigned>(grid)), dim3(TC_THREADS), smem, s, wmap, dmap,
                       p);

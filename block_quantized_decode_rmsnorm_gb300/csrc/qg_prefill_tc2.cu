@@ -28,7 +28,6 @@
 // Every barrier wait is bounded by the global timer; a stalled pipeline aborts
 // (NaN outputs for the tiles left) instead of hanging.
 #include <cuda.h>
-#include <mutex>
 
 #include "qg_common.cuh"
 #include "qg_tc.cuh"
@@ -414,13 +413,10 @@ static cudaError_t launch_tc2_bn(EncodeTiledFn enc, const uint16_t *w_codes, con
     p.k = static_cast<int>(k);
     p.m_tiles = (m + T2_BM - 1) / T2_BM;
     p.tiles = p.m_tiles * ((n + BN - 1) / BN);
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(prefill_tc2_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaError_t e = opt_in_smem(reinterpret_cast<const void *>(prefill_tc2_kernel<BN>),
                                     static_cast<int>(T2Layout<BN>::BYTES + 1024));
-    });
-    if (attr != cudaSuccess) return attr;
+        e != cudaSuccess)
+        return e;
     const int64_t grid = p.tiles < num_sms() ? p.tiles : num_sms();
     return launch_pdl(prefill_tc2_kernel<BN>, dim3(static_cast<unsigned>(grid)), dim3(L::THREADS),
                       static_cast<size_t>(L::BYTES + 1024), s, mx, mw, mdx, mdw, p);
