@@ -50,6 +50,48 @@ def test_status_strings(lib):
     assert lib.qg_status_str(99) == b"unknown status"
 
 
+def test_boundary_is_usable_from_c(lib, tmp_path):
+    """The header is ISO C11 (warnings as errors, -pedantic), and a C program
+    linked against the library gets its status codes back.  Argument errors
+    only, so no GPU is needed."""
+    import shutil
+    import subprocess
+
+    from block_quantized_decode_rmsnorm_gb300 import _lib
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_qgemv.c"
+    src.write_text(r"""
+#include <stdint.h>
+#include <stdio.h>
+#include "qgemv.h"
+#define FAKE ((void *)(uintptr_t)0x100000) /* well aligned, never dereferenced */
+int main(void)
+{
+    if (qg_abi_version() != 1) return 1;
+    /* k not a multiple of 32 */
+    if (qgemv_q8_0(FAKE, FAKE, 8, 48, FAKE, FAKE, 1, QG_EPI_NONE, NULL, FAKE, NULL) != QG_ERR_SHAPE) return 2;
+    /* a required pointer missing */
+    if (quantize_act_q8_0(NULL, 1, 32, FAKE, FAKE, NULL) != QG_ERR_NULL) return 3;
+    /* nothing to do */
+    if (qgemm_q8_0_prefill_tc2(NULL, NULL, 0, 256, NULL, NULL, 0, NULL, 0, NULL) != QG_OK) return 4;
+    printf("%s|%s\n", qg_status_str(QG_ERR_ALIGN), qg_status_str(QG_OK));
+    return 0;
+}
+""")
+    exe = tmp_path / "use_qgemv"
+    libdir = os.path.dirname(_lib.LIB_PATH)
+    cudalib = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "lib64")
+    subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-pedantic", "-Werror", f"-I{os.path.join(ROOT, 'include')}",
+                    str(src), "-o", str(exe), f"-L{libdir}", "-lqgemv", f"-Wl,-rpath,{libdir}",
+                    f"-Wl,-rpath-link,{cudalib}"], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, out
+    assert out.stdout.strip() == f"{lib.qg_status_str(2).decode()}|{lib.qg_status_str(0).decode()}"
+
+
 FAKE = 1 << 20  # a well-aligned, never-dereferenced address
 
 
