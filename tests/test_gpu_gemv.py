@@ -44,6 +44,20 @@ SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("batch", [1, 3])
+def test_gemv_longest_guaranteed_k(torch, orc, batch):
+    """K = 2^17 (4096 blocks; ragged row count): the longest reduction for which
+    the accumulation bound, (ceil(nb / 32) + 6) 2^-24 A, stays inside the
+    normalised tolerance."""
+    from block_quantized_decode_rmsnorm_gb300 import api
+
+    n, k = 37, 1 << 17
+    qs, d, xq, xd = _case(orc, 17 + batch, n, k, batch)
+    y = _run(torch, api, qs, d, xq, xd, "none")
+    y64, a64 = orc.gemv_q8_0(qs, d, xq, xd)
+    assert_close(y, y64, a64, TOL_Q8, f"gemv n={n} k={k} b={batch}")
+
+
 @pytest.mark.parametrize("n,k,batch", SHAPES)
 def test_gemv_none(torch, orc, n, k, batch):
     from block_quantized_decode_rmsnorm_gb300 import api
