@@ -4,17 +4,21 @@
 Headline workload: the decode feed-forward block of a 0.8B-shaped model (hidden
 1024, stacked gate|up 7168 x 1024, down 1024 x 3584, Q8_0 weights), batch 1.
 One step = one decode step's worth of that block: L chained layers (default 24)
-with distinct weights, replayed as one CUDA graph (RMSNorm+quantize, gate|up
-GEMV with SiLU*u, quantize, down GEMV with the residual folded in: 4 launches per
-layer).  The weights of one step (L x 11.7 MB) exceed the L2 cache, so every step
-streams them from HBM.
+with distinct weights, replayed as one CUDA graph.  Each layer is two launches
+(--path two, the default): RMSNorm + Q8_0 of x + stacked gate|up + SiLU*u + Q8_0
+of h in one kernel, then the down GEMV with the residual folded in.  --path four
+runs the same layer unfused (4 launches), --path one as one launch per layer.
+The weights of one step (L x 11.7 MB) exceed the L2 cache, so every step streams
+them from HBM.
 
 Metric: achieved HBM GB/s = algorithmic bytes of the step / step time.  The line
-also carries the roofline of the dominant kernel (the gate|up GEMV), an
-end-to-end number through host buffers, the CPU oracle timed on the host, the SM
-clocks sampled during the timed region, and (unless --quick) the other
-workloads' kernel rates: Q8_0 GEMV 256x1024, bf16 projection 18432x2560,
-output-head GEMV 262144x1024 at batch 1/2/4/8, and the M=512 prompt contraction.
+also carries the roofline of the dominant kernel (the fused gate|up kernel), an
+end-to-end number through pinned host buffers (input read and result written by
+the first and last layers, the host waiting every step), the CPU oracle timed on
+the host, the SM clocks sampled during the timed region, and (unless --quick) the
+other workloads' kernel rates: Q8_0 GEMV 256x1024, bf16 projection 18432x2560,
+output-head GEMV 262144x1024 at batch 1/2/4/8, the bf16 and Q8_0 prompt
+contractions for 512 rows, and the int8 mma.sync rate.
 
 --impl reference times the CPU oracle (the only reference this method has) on
 the same workload and prints the same line with "impl": "reference".
