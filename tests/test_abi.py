@@ -50,7 +50,7 @@ def test_status_strings(lib):
     assert lib.qg_status_str(99) == b"unknown status"
 
 
-def test_boundary_is_usable_from_c(lib, tmp_path):
+def test_boundary_is_usable_from_c(lib):
     """The header is ISO C11 (warnings as errors, -pedantic), and a C program
     linked against the library gets its status codes back.  Argument errors
     only, so no GPU is needed."""
@@ -62,7 +62,11 @@ def test_boundary_is_usable_from_c(lib, tmp_path):
     gcc = shutil.which("gcc")
     if gcc is None:
         pytest.skip("no C compiler")
-    src = tmp_path / "use_qgemv.c"
+    from pathlib import Path
+
+    work = Path(ROOT) / "block_quantized_decode_rmsnorm_gb300" / "_build" / "c_abi_check"  # git-ignored
+    work.mkdir(parents=True, exist_ok=True)
+    src = work / "use_qgemv.c"
     src.write_text(r"""
 #include <stdint.h>
 #include <stdio.h>
@@ -81,7 +85,7 @@ int main(void)
     return 0;
 }
 """)
-    exe = tmp_path / "use_qgemv"
+    exe = work / "use_qgemv"
     libdir = os.path.dirname(_lib.LIB_PATH)
     cudalib = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "lib64")
     subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-pedantic", "-Werror", f"-I{os.path.join(ROOT, 'include')}",
