@@ -50,6 +50,20 @@ def test_status_strings(lib):
     assert lib.qg_status_str(99) == b"unknown status"
 
 
+def test_binding_scale_planes_match_the_library_stride(lib):
+    """F16Codes allocates its block-major scale plane with the library's row
+    stride (qg_scales_ld), for every residue of the row count."""
+    torch = pytest.importorskip("torch")
+    from block_quantized_decode_rmsnorm_gb300.api import F16Codes
+
+    for rows in (1, 2, 3, 4, 5, 37, 128, 7169):
+        c = F16Codes.empty(rows, 64, "cpu")
+        assert c.codes.shape == (rows, 64) and c.codes.dtype == torch.float16
+        assert c.scales_t.shape == (2, lib.qg_scales_ld(rows))
+        with pytest.raises(ValueError):  # the library's kernels only read device memory here
+            c.check("x")
+
+
 def test_boundary_is_usable_from_c(lib):
     """The header is ISO C11 (warnings as errors, -pedantic), and a C program
     linked against the library gets its status codes back.  Argument errors
