@@ -69,6 +69,8 @@ def _load():
                 "orc_gemv_q8_0": (None, [P, P, I64, I64, P, P, I64, P, P]),
                 "orc_silu_mul": (None, [P, P, I64, P]),
                 "orc_gemv_bf16": (None, [P, I64, I64, P, P, F, P, P, P, P]),
+                "orc_residual_add": (None, [P, P, I64, P]),
+                "orc_decode_ffn": (None, [P, P, I64, I64, F, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -230,24 +232,51 @@ def gemv_bf16(w_bits, x_bits, gamma_bits, eps: float):
 # composite steps, in the pages' order
 # --------------------------------------------------------------------------
 
+def residual_add(res, y) -> np.ndarray:
+    """out f64[n] = res (f32) + y (f64)."""
+    lib = _load()
+    r = _c(res, np.float32).ravel()
+    y = _c(y, np.float64).ravel()
+    out = np.empty(r.size, np.float64)
+    lib.orc_residual_add(_ptr(r), _ptr(y), r.size, _ptr(out))
+    return out
+
+
 def decode_ffn(x, gamma, eps, gu_qs, gu_d, dn_qs, dn_d):
-    """One decode FFN: RMSNorm -> Q8_0 -> stacked gate|up -> SiLU(g)*u -> Q8_0 -> down + x.
+    """One decode FFN: RMSNorm -> Q8_0 -> stacked gate|up -> SiLU(g)*u -> Q8_0 -> down + x
+    (orc_decode_ffn, every step in C).
 
     Returns a dict with every intermediate: f64 exact values ("*64"), their
     magnitude sums ("a_*"), and the f32 values the step hands on ("h", "out").
     """
-    q, d, r, xh = rmsnorm_quantize(x, gamma, eps)
-    gu, a_gu = gemv_q8_0(gu_qs, gu_d, q, d)
-    F = gu_qs.shape[0] // 2
-    g, u = gu[0, :F], gu[0, F:]
-    h64 = silu_mul(g, u)
-    h = h64.astype(np.float32)
-    hq, hd = quantize_q8_0(h)
-    y, a_y = gemv_q8_0(dn_qs, dn_d, hq, hd)
-    out64 = np.asarray(x, np.float64) + y[0]
+    lib = _load()
+    x = _c(x, np.float32).ravel()
+    g = _c(gamma, np.float32).ravel()
+    gq, gd = _c(gu_qs, np.int8), _c(gu_d, np.uint16)
+    dq, dd = _c(dn_qs, np.int8), _c(dn_d, np.uint16)
+    k = x.size
+    F = gq.shape[0] // 2
+    if g.size != k or gq.shape != (2 * F, k) or gd.shape != (2 * F, k // 32) or dq.shape != (k, F) \
+            or dd.shape != (k, F // 32):
+        raise ValueError("bad shapes")
+    xq = np.empty(k, np.int8)
+    xd = np.empty(k // 32, np.uint16)
+    r = np.zeros(1, np.float32)
+    gu = np.empty(2 * F, np.float64)
+    a_gu = np.empty(2 * F, np.float64)
+    h64 = np.empty(F, np.float64)
+    h = np.empty(F, np.float32)
+    hq = np.empty(F, np.int8)
+    hd = np.empty(F // 32, np.uint16)
+    y = np.empty(k, np.float64)
+    a_y = np.empty(k, np.float64)
+    out64 = np.empty(k, np.float64)
+    lib.orc_decode_ffn(_ptr(x), _ptr(g), k, F, eps, _ptr(gq), _ptr(gd), _ptr(dq), _ptr(dd), _ptr(xq), _ptr(xd),
+                       _ptr(r), _ptr(gu), _ptr(a_gu), _ptr(h64), _ptr(h), _ptr(hq), _ptr(hd), _ptr(y), _ptr(a_y),
+                       _ptr(out64))
     return {
-        "xq": q, "xd": d, "r": r, "xhat": xh,
-        "gu64": gu[0], "a_gu": a_gu[0], "h64": h64, "h": h,
-        "hq": hq, "hd": hd, "y64": y[0], "a_y": a_y[0],
+        "xq": xq, "xd": xd, "r": r[0],
+        "gu64": gu, "a_gu": a_gu, "h64": h64, "h": h,
+        "hq": hq[None, :], "hd": hd[None, :], "y64": y, "a_y": a_y,
         "out64": out64, "out": out64.astype(np.float32),
     }

@@ -327,6 +327,47 @@ void orc_silu_mul(const double *g, const double *u, int64_t n, double *h)
         h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];
 }
 
+/* Residual folded into the last product ([Phobos] Fast Decode): out[n] =
+ * res[n] + y[n] in f64 (res is f32, so exact in f64; y is the exact f64 value of
+ * the block-scaled sum). */
+void orc_residual_add(const float *res, const double *y, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = (double)res[i] + y[i];
+}
+
+/* One decode feed-forward block, every step in the pages' order ([Phobos] Fast
+ * Decode: quantize the activation once and share it between the stacked
+ * projections, fold the residual add into the last matmul; [Herbert] Emitting
+ * for a GPU: norm in front of the stacked gate|up, activation behind it):
+ *   q, d   = Q8_0(RMSNorm(x) * gamma)                    (orc_rmsnorm_quantize)
+ *   g | u  = stacked gate|up rows [0, F) | [F, 2F)        (orc_gemv_q8_0, f64)
+ *   h      = f32(silu(g) * u)                             (orc_silu_mul, then one f32 rounding)
+ *   hq, hd = Q8_0(h)                                      (orc_quantize_q8_0)
+ *   out    = x + down(hq, hd)                             (orc_gemv_q8_0, orc_residual_add)
+ * Outputs (caller-allocated): xq int8[k], xd u16[k/32], r f32[1], gu f64[2F],
+ * a_gu f64[2F], h64 f64[F], h f32[F], hq int8[F], hd u16[F/32], y f64[k],
+ * a_y f64[k], out f64[k]. */
+void orc_decode_ffn(const float *x, const float *gamma, int64_t k, int64_t ffn, float eps,
+                    const int8_t *gu_qs, const uint16_t *gu_d, const int8_t *dn_qs,
+                    const uint16_t *dn_d, int8_t *xq, uint16_t *xd, float *r, double *gu,
+                    double *a_gu, double *h64, float *h, int8_t *hq, uint16_t *hd, double *y,
+                    double *a_y, double *out)
+{
+    float *xhat = (float *)calloc((size_t)k, sizeof(float));
+    if (!xhat)
+        return;
+    orc_rmsnorm_quantize(x, gamma, k, eps, xq, xd, r, xhat);
+    free(xhat);
+    orc_gemv_q8_0(gu_qs, gu_d, 2 * ffn, k, xq, xd, 1, gu, a_gu);
+    orc_silu_mul(gu, gu + ffn, ffn, h64);
+    for (int64_t i = 0; i < ffn; ++i)
+        h[i] = (float)h64[i];
+    orc_quantize_q8_0(h, 1, ffn, hq, hd);
+    orc_gemv_q8_0(dn_qs, dn_d, k, ffn, hq, hd, 1, y, a_y);
+    orc_residual_add(x, y, k, out);
+}
+
 /* ------------------------------------------------------------------------ */
 /* bf16 projection with the norm in front                                     */
 /* ------------------------------------------------------------------------ */
