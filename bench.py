@@ -49,6 +49,11 @@ W_DN_BYTES = HIDDEN * FFN + HIDDEN * (FFN // 32) * 2
 LAYER_BYTES = W_GU_BYTES + W_DN_BYTES + 3 * HIDDEN * 4
 # fused gate|up launch: weights, x and gamma in (f32), h out (f32) and its Q8_0 codes + scales
 GU_KERNEL_BYTES = W_GU_BYTES + 2 * HIDDEN * 4 + FFN * 4 + FFN + (FFN // 32) * 2
+# persistent stack kernel over n layers: every layer's weights and gain, the input and the output row
+def STACK_KERNEL_BYTES(n: int) -> int:
+    return n * (W_GU_BYTES + W_DN_BYTES + HIDDEN * 4) + 2 * HIDDEN * 4
+
+
 # one-launch layer: both weights, x in, gamma, x out, the cleared buffer, h and its codes and scales
 LAYER_KERNEL_BYTES = W_GU_BYTES + W_DN_BYTES + 4 * HIDDEN * 4 + FFN * 4 + FFN + (FFN // 32) * 2
 
@@ -408,7 +413,7 @@ def ncu_traffic(kernel_key: str):
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("qg_ffn.cu", "qg_norm.cuh", "qg_common.cuh"):
+    for f in ("qg_ffn.cu", "qg_stack.cu", "qg_norm.cuh", "qg_common.cuh"):
         with open(os.path.join(ROOT, "block_quantized_decode_rmsnorm_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
@@ -472,10 +477,15 @@ def run_ours(args):
     x = torch.from_numpy(x0_np).cuda()
 
     path = args.path
-    launches_per_layer = {"one": 1, "two": 2, "four": 4}[path]
-    launches_per_step = launches_per_layer * L + (1 if path == "one" else 0)  # + the finish
+    if path == "stack":
+        launches_per_step = -(-L // api._lib.load().qg_decode_stack_max_layers())
+    else:
+        launches_per_step = {"one": 1, "two": 2, "four": 4}[path] * L + (1 if path == "one" else 0)  # + the finish
     stack = api.LayerStack(HIDDEN, FFN, "cuda") if path == "one" else None
+    dstack = api.DecodeStack(layers) if path == "stack" else None
     x_out = x
+    if dstack is not None:
+        x_out = torch.empty_like(x)  # each replay reads x and writes x_out
     if stack is not None:
         for layer in layers:  # down weights in the column-block layout, packed once at load time
             api.prepare_one_launch(layer)
@@ -484,6 +494,9 @@ def run_ours(args):
         x, x_out = stack.r[0], stack.out  # each replay reads r[0] and writes out
 
     def step():
+        if dstack is not None:
+            dstack.run(x, x_out, EPS)
+            return
         if stack is not None:
             stack.run(layers, buf, EPS)
             return
@@ -515,7 +528,13 @@ def run_ours(args):
     value = job_rate(dist.world, args.steps, step_bytes, elapsed)
 
     # dominant kernel, timed alone (L back-to-back launches in a graph, events on the launching stream)
-    if path == "one":
+    if path == "stack":
+        # the persistent kernel is the whole step: time it over back-to-back replays
+        t_k = time_graph(torch, g, max(5, args.steps // 4)) / launches_per_step
+        kbytes = STACK_KERNEL_BYTES(min(L, api._lib.load().qg_decode_stack_max_layers()))
+        kname, kkey = ("decode_stack_kernel (every layer in one cooperative launch: RMSNorm + Q8_0 + gate|up + SiLU*u "
+                       "+ Q8_0 + down + residual, hand-offs through value+epoch words)"), "decode_stack_kernel"
+    elif path == "one":
         # the layer kernel is the step's only kernel but the one-block finish
         t_k = time_graph(torch, g, max(5, args.steps // 4)) / L
         kbytes, kname, kkey = LAYER_KERNEL_BYTES, ("ffn_up_kernel<1,true> (one-launch layer: RMSNorm + Q8_0 + "
@@ -541,9 +560,12 @@ def run_ours(args):
     # result out with copies captured in the graph.
     x_host = torch.from_numpy(x0_np.copy()).pin_memory()
     out_host = torch.empty_like(x_host).pin_memory()
-    direct = path == "two" and stack is None
+    direct = path in ("two", "stack") and stack is None
 
     def e2e_step():
+        if dstack is not None:
+            dstack.run(x_host, out_host, EPS)
+            return
         if direct:
             src = x_host
             for i, layer in enumerate(layers):
@@ -581,7 +603,8 @@ def run_ours(args):
                    "l2": f"inputs larger than L2: {step_bytes / 1e6:.0f} MB of weights per step, "
                          f"L2 {torch.cuda.get_device_properties(dev).L2_cache_size / 1e6:.0f} MB",
                    "graph": f"one CUDA graph per step, {launches_per_step} launches, programmatic dependent launch",
-                   "path": {"one": "one launch per layer (qg_decode_layer_q8_0: split-K down, cluster partials summed by the next layer) + finish",
+                   "path": {"stack": "every layer in one persistent cooperative launch (qg_decode_stack_q8_0)",
+                            "one": "one launch per layer (qg_decode_layer_q8_0: split-K down, cluster partials summed by the next layer) + finish",
                             "two": "two launches per layer (qg_decode_ffn_q8_0)",
                             "four": "four launches per layer (decode_ffn_q8_0)"}[path],
                    "parallelism": f"replicas x{dist.world} (independent decode streams, no collective)"},
@@ -710,8 +733,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layers", type=int, default=24)
     ap.add_argument("--quick", action="store_true", help="skip the other workloads' kernel rates")
-    ap.add_argument("--path", choices=["one", "two", "four"], default="two",
-                    help="launches per decode layer: one (split-K down inside the layer kernel), two, four")
+    ap.add_argument("--path", choices=["stack", "one", "two", "four"], default="two",
+                    help="stack: every layer in one persistent launch; otherwise launches per decode layer: one "
+                         "(split-K down inside the layer kernel), two, four")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--workload", choices=["prefill", "prefill_wide", "prefill_bf16", "head1", "head2", "head4", "head8", "bf16"],
                     help="time one workload's kernel alone (for profiling) instead of the bench step")

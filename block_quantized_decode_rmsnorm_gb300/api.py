@@ -603,6 +603,89 @@ def qg_decode_layers_q8_0_noalloc(x_in: torch.Tensor, layers, eps: float = 1e-6,
     return x_out
 
 
+def qg_decode_stack_workspace_bytes(hidden: int, ffn: int) -> int:
+    n = _lib.load().qg_decode_stack_workspace_bytes(hidden, ffn)
+    if n < 0:
+        raise ValueError(f"persistent decode stack: unsupported shape hidden={hidden} ffn={ffn}")
+    return n
+
+
+class DecodeStack:
+    """Decode FFN layers run as one persistent launch per up to
+    qg_decode_stack_max_layers() layers (qg_decode_stack_q8_0).
+
+    "Filling in the blanks: Inference using Phobos", Q4_K_M: the whole MLP as
+    one persistent kernel.  Owns the zero-filled workspace the launches share
+    and the host arrays of the layers' device pointers; allocates nothing after
+    construction, so run() can be captured into a CUDA graph.
+    """
+
+    def __init__(self, layers, device="cuda"):
+        import ctypes
+
+        self.layers = list(layers)
+        if not self.layers:
+            raise ValueError("DecodeStack needs at least one layer")
+        self.hidden = self.layers[0].gamma.shape[-1]
+        self.ffn = self.layers[0].down.k
+        for ly in self.layers:
+            _need(ly.gamma, "gamma", torch.float32, (self.hidden,))
+            _need(ly.gate_up.qs, "gate_up.qs", torch.int8, (2 * self.ffn, self.hidden))
+            _need(ly.gate_up.d, "gate_up.d", torch.float16, (2 * self.ffn, self.hidden // 32))
+            _need(ly.down.qs, "down.qs", torch.int8, (self.hidden, self.ffn))
+            _need(ly.down.d, "down.d", torch.float16, (self.hidden, self.ffn // 32))
+        self.workspace = torch.zeros(qg_decode_stack_workspace_bytes(self.hidden, self.ffn), dtype=torch.uint8,
+                                     device=device)
+        self.chunk = _lib.load().qg_decode_stack_max_layers()
+        self._arrays = []  # per chunk: (n, gamma, wgu_qs, wgu_d, wdn_qs, wdn_d) host pointer arrays
+        for c0 in range(0, len(self.layers), self.chunk):
+            ch = self.layers[c0:c0 + self.chunk]
+            arr = lambda vals: (ctypes.c_void_p * len(vals))(*vals)
+            self._arrays.append((len(ch), arr([ly.gamma.data_ptr() for ly in ch]),
+                                 arr([ly.gate_up.qs.data_ptr() for ly in ch]),
+                                 arr([ly.gate_up.d.data_ptr() for ly in ch]),
+                                 arr([ly.down.qs.data_ptr() for ly in ch]),
+                                 arr([ly.down.d.data_ptr() for ly in ch])))
+
+    def run(self, x_in: torch.Tensor, x_out: torch.Tensor | None = None, eps: float = 1e-6, h_last=None,
+            hq_last=None, hd_last=None, wait_limit_ns: int = 0, stream=None) -> torch.Tensor:
+        """x_out <- the stack applied to x_in (either may be pinned host memory;
+        x_out may be x_in).  h_last / hq_last / hd_last receive the last layer's
+        activation and its Q8_0 codes and scales when given."""
+        _need_reachable(x_in, "x_in", (self.hidden,))
+        if x_out is None:
+            x_out = torch.empty_like(x_in)
+        _need_reachable(x_out, "x_out", (self.hidden,))
+        if h_last is not None:
+            _need(h_last, "h_last", torch.float32, (self.ffn,))
+        if hq_last is not None:
+            _need(hq_last, "hq_last", torch.int8, (self.ffn,))
+        if hd_last is not None:
+            _need(hd_last, "hd_last", torch.float16, (self.ffn // 32,))
+        s = _stream_handle(stream)
+        src = x_in
+        for i, (n, g, gq, gd, dq, dd) in enumerate(self._arrays):
+            last = i == len(self._arrays) - 1
+            _lib.call("qg_decode_stack_q8_0", src.data_ptr(), x_out.data_ptr(), n, g, gq, gd, dq, dd, self.hidden,
+                      self.ffn, float(eps), self.workspace.data_ptr(), _ptr(h_last) if last else None,
+                      _ptr(hq_last) if last else None, _ptr(hd_last) if last else None, int(wait_limit_ns), s)
+            src = x_out
+        return x_out
+
+    def status(self) -> int:
+        """The workspace status word (0: every launch since the last reset completed
+        normally).  Waits for the device."""
+        return int(self.workspace[:4].view(torch.int32).item())
+
+    def generation(self) -> int:
+        """Launches completed on this workspace since the last reset (mod 2^32)."""
+        return int(self.workspace[4:8].view(torch.int32).item()) & 0xFFFFFFFF
+
+    def reset(self) -> None:
+        """Zero-fill the workspace again (after a launch that set the status)."""
+        self.workspace.zero_()
+
+
 # --------------------------------------------------------------------------
 # host <-> device helpers (plumbing)
 # --------------------------------------------------------------------------

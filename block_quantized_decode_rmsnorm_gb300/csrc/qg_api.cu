@@ -50,6 +50,16 @@ cudaError_t launch_prefill_tc(const int8_t *, const uint16_t *, int64_t, int64_t
                               cudaStream_t);
 cudaError_t launch_gemv_prefetch(const int8_t *, const uint16_t *, int64_t, int64_t, const int8_t *, const uint16_t *,
                                  int, const float *, float *, cudaStream_t);
+struct StackShape {
+    int rows_b, grid;
+    size_t smem;
+};
+bool stack_shape(int64_t k, int64_t ffn, StackShape *out);
+size_t stack_workspace_bytes(int64_t k, int64_t ffn);
+int stack_max_layers();
+cudaError_t launch_decode_stack(const float *, float *, int, const float *const *, const int8_t *const *,
+                                const uint16_t *const *, const int8_t *const *, const uint16_t *const *, int64_t,
+                                int64_t, float, void *, float *, int8_t *, uint16_t *, uint64_t, cudaStream_t);
 
 // SM count of the current device, read once per device.
 int num_sms()
@@ -375,6 +385,48 @@ qg_status qg_decode_layers_q8_0_noalloc(const float *x_in, float *x_out, int32_t
     }
     return from_cuda(qg::launch_decode_layers_noalloc(x_in, x_out, n_layers, gamma, wgu_qs, wgu_d, wdn_qs, wdn_d,
                                                       hidden, ffn, eps, stream));
+}
+
+int64_t qg_decode_stack_workspace_bytes(int64_t hidden, int64_t ffn)
+{
+    if (!layer_shape_ok(hidden, ffn) || !qg::stack_shape(hidden, ffn, nullptr)) return -1;
+    return static_cast<int64_t>(qg::stack_workspace_bytes(hidden, ffn));
+}
+
+int32_t qg_decode_stack_max_layers(void) { return qg::stack_max_layers(); }
+
+qg_status qg_decode_stack_q8_0(const float *x_in, float *x_out, int32_t n_layers, const float *const *gamma,
+                               const int8_t *const *wgu_qs, const uint16_t *const *wgu_d,
+                               const int8_t *const *wdn_qs, const uint16_t *const *wdn_d, int64_t hidden,
+                               int64_t ffn, float eps, void *workspace, float *h_last, int8_t *hq_last,
+                               uint16_t *hd_last, int64_t wait_limit_ns, qg_stream_t stream)
+{
+    if (!layer_shape_ok(hidden, ffn) || n_layers < 1 || n_layers > qg::stack_max_layers() || !(eps >= 0.0f) ||
+        wait_limit_ns < 0)
+        return QG_ERR_SHAPE;
+    if (!qg::stack_shape(hidden, ffn, nullptr)) return QG_ERR_UNSUPPORTED;
+    if (!x_in || !x_out || !workspace || !gamma || !wgu_qs || !wgu_d || !wdn_qs || !wdn_d) return QG_ERR_NULL;
+    if (!aligned(x_in, 16) || !aligned(x_out, 4) || !aligned(workspace, 256) || !aligned(h_last, 4) ||
+        !aligned(hd_last, 2))
+        return QG_ERR_ALIGN;
+    for (int32_t l = 0; l < n_layers; ++l) {
+        if (!gamma[l] || !wgu_qs[l] || !wgu_d[l] || !wdn_qs[l] || !wdn_d[l]) return QG_ERR_NULL;
+        if (!aligned(gamma[l], 16) || !aligned(wgu_qs[l], 32) || !aligned(wgu_d[l], 16) || !aligned(wdn_qs[l], 32) ||
+            !aligned(wdn_d[l], 16))
+            return QG_ERR_ALIGN;
+    }
+    const size_t xb = static_cast<size_t>(hidden) * 4, wb = qg::stack_workspace_bytes(hidden, ffn);
+    // in place or apart (each down row reads its residual before it writes the
+    // row); nothing may overlap the workspace, which every CTA reads and writes
+    if (x_in != x_out && overlap(x_in, xb, x_out, xb)) return QG_ERR_SHAPE;
+    if (overlap(x_in, xb, workspace, wb) || overlap(x_out, xb, workspace, wb)) return QG_ERR_SHAPE;
+    const size_t fb = static_cast<size_t>(ffn);
+    if ((h_last && overlap(h_last, fb * 4, workspace, wb)) || (hq_last && overlap(hq_last, fb, workspace, wb)) ||
+        (hd_last && overlap(hd_last, fb / 16, workspace, wb)))
+        return QG_ERR_SHAPE;
+    const uint64_t limit = wait_limit_ns == 0 ? qg::kCopyWaitLimitNs : static_cast<uint64_t>(wait_limit_ns);
+    return from_cuda(qg::launch_decode_stack(x_in, x_out, n_layers, gamma, wgu_qs, wgu_d, wdn_qs, wdn_d, hidden, ffn,
+                                             eps, workspace, h_last, hq_last, hd_last, limit, stream));
 }
 
 qg_status qgemm_q8_0_prefill_tc(const int8_t *w_qs, const uint16_t *w_d, int64_t n_rows, int64_t k, const void *xt,

@@ -32,9 +32,10 @@ cudaError_t launch_decode_layer(const float *, const float *, int, float *, floa
 cudaError_t launch_layer_finish(const float *, const float *, int, int64_t, float *, cudaStream_t);
 int decode_layer_partials(int64_t half);
 
-// 256 KB: enough for hidden 1024 with up to 16 partial vectors and ffn up to
-// 8192 (the 0.8B shape, hidden 1024 / ffn 3584, takes 141,056 B); the largest
-// supported shapes (hidden 1792 with 16 partials) do not fit and are refused.
+// 256 KB: enough for every ffn the one-launch layer serves at hidden 1024 (up
+// to 4096, i.e. 16 partial vectors from clusters of 8: 160,000 B; the 0.8B
+// shape, hidden 1024 / ffn 3584, takes 141,056 B); the largest shapes it serves
+// (hidden 1792 with 16 partials: 264,448 B) do not fit and are refused.
 constexpr size_t kLayerScratchBytes = 256 * 1024;
 static __device__ __align__(256) uint8_t g_layer_scratch[kLayerScratchBytes];
 

@@ -31,9 +31,16 @@
  *   completed are fine).
  * - Errors: argument errors are returned before anything is launched; a
  *   launch failure returns QG_ERR_CUDA.  Errors inside the kernels are not
- *   reported by these calls (the kernels have no failing paths on valid input).
+ *   reported by these calls (the kernels have no failing paths on valid input),
+ *   except by qg_decode_stack_q8_0, whose workspace holds a status word.
  * - Outputs never alias inputs, except where a call says so.
- * - Thread-safe; no global state.
+ * - Threads and state: calls may be made from several host threads.  The
+ *   library keeps per-device caches, filled on first use under a lock (the SM
+ *   count, the shared-memory opt-in of each kernel).  Two entry points share
+ *   device memory between calls: qg_decode_layers_q8_0_noalloc uses one fixed
+ *   array per GPU compiled into the library, and qg_decode_stack_q8_0 a
+ *   caller-owned workspace.  Calls that share that array, or a workspace, must
+ *   not overlap in time; every other call is independent of every other.
  */
 #ifndef QGEMV_H
 #define QGEMV_H
@@ -341,6 +348,58 @@ QG_API qg_status qg_decode_layers_q8_0_noalloc(const float *x_in, float *x_out, 
                                                const int8_t *const *wdn_qs, const uint16_t *const *wdn_d,
                                                int64_t hidden, int64_t ffn, float eps,
                                                qg_stream_t stream);
+
+/*
+ * qg_decode_stack_q8_0 - n_layers decode feed-forward blocks, each
+ *   x <- x + down(Q8_0(SiLU(g) * u)),  (g|u) = gate|up(Q8_0(RMSNorm(x) * gamma)),
+ * in ONE persistent launch ([Phobos] Q4_K_M: the whole MLP as one persistent
+ * kernel; Fast Decode: quantize the activation once and share it, stack the
+ * projections, fold the residual into the matmul; [Herbert] Emitting for a GPU:
+ * fuse the normalization and the activation with the projections around them).
+ * One CTA per SM, launched cooperatively (all resident at once); each layer's
+ * two all-to-all steps (all of x before the gate|up rows, all of h before the
+ * down rows) are hand-offs through workspace words that hold a value and an
+ * epoch, polled by the consumers, instead of kernel boundaries; the weights of
+ * the next layers stream into shared memory while a layer computes.  The
+ * result has the same bits as n_layers calls of qg_decode_ffn_q8_0_out.
+ *   x_in:  f32[hidden], 16-byte aligned: device or pinned host memory (read)
+ *   x_out: f32[hidden]: device or pinned host memory (written); x_in itself,
+ *          or not overlapping it (QG_ERR_SHAPE otherwise)
+ *   gamma, wgu_qs, wgu_d, wdn_qs, wdn_d: HOST arrays of n_layers DEVICE
+ *          pointers, one set per layer, read during the call only: gains
+ *          f32[hidden] (16-byte aligned), stacked gate|up planes [2*ffn][hidden],
+ *          down planes [hidden][ffn] (row-major, as qg_decode_ffn_q8_0; values
+ *          32-byte, scales 16-byte aligned)
+ *   n_layers: 1 .. qg_decode_stack_max_layers() (QG_ERR_SHAPE otherwise);
+ *          chain calls for more layers (x_out of one as x_in of the next)
+ *   workspace: device memory of qg_decode_stack_workspace_bytes(hidden, ffn)
+ *          bytes, 256-byte aligned, ZERO-FILLED before its first use and then
+ *          left to the library; one workspace serves one shape; calls that
+ *          share a workspace must not overlap in time (one stream).  Its first
+ *          32-bit word is the status: 0 while every launch since it was zeroed
+ *          completed normally; bit 0 set when a hand-off wait ran past
+ *          wait_limit_ns (or saw another CTA give up), bit 1 when a weight copy
+ *          did not land in time.  A launch that sets it returns normally with
+ *          x_out (and h_last) undefined; the status stays set until the
+ *          workspace is zero-filled again.
+ *   h_last, hq_last, hd_last: optional (NULL): the last layer's h f32[ffn]
+ *          (4-byte aligned), its Q8_0 codes int8[ffn] and scales binary16[ffn/32]
+ *   wait_limit_ns: bound on every wait inside the kernel; 0 = one second
+ *   Shapes: hidden a multiple of 256 up to 1024, ffn a multiple of 256 up to
+ *   4096 with ffn/32 at most the SM count, and both layers' weight slabs within
+ *   one CTA's shared memory (QG_ERR_UNSUPPORTED otherwise; the 0.8B shape,
+ *   hidden 1024 / ffn 3584, is served).  A failed cooperative launch (e.g. SMs
+ *   held by other work) returns QG_ERR_CUDA.
+ */
+QG_API int64_t qg_decode_stack_workspace_bytes(int64_t hidden, int64_t ffn); /* -1: unsupported */
+QG_API int32_t qg_decode_stack_max_layers(void);
+QG_API qg_status qg_decode_stack_q8_0(const float *x_in, float *x_out, int32_t n_layers,
+                                      const float *const *gamma,
+                                      const int8_t *const *wgu_qs, const uint16_t *const *wgu_d,
+                                      const int8_t *const *wdn_qs, const uint16_t *const *wdn_d,
+                                      int64_t hidden, int64_t ffn, float eps, void *workspace,
+                                      float *h_last, int8_t *hq_last, uint16_t *hd_last,
+                                      int64_t wait_limit_ns, qg_stream_t stream);
 
 /*
  * qgemm_q8_0_prefill_tc - the prompt contraction of qgemm_q8_0_prefill on the

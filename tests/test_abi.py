@@ -281,8 +281,14 @@ def test_noalloc_stack_argument_errors(lib):
     f = lib.qg_decode_layers_q8_0_noalloc
     eps = ctypes.c_float(1e-6)
     arr = (ctypes.c_void_p * 1)(FAKE)
-    # intermediates larger than the fixed scratch array: refused before any launch
+    # intermediates larger than the fixed scratch array: refused before any launch.
+    # The one-launch layer itself serves this shape (16 partials), so the refusal
+    # is the scratch array's, not the layer's.
+    assert lib.qg_decode_layer_partials(1792, 4096) == 16
     assert f(FAKE, FAKE, 1, arr, arr, arr, arr, arr, 1792, 4096, eps, None) == 4
+    # the largest ffn the one-launch layer serves at hidden 1024 fits the array
+    assert lib.qg_decode_layer_partials(1024, 4096) == 16
+    assert lib.qg_decode_layer_partials(1024, 4096 + 256) == -1
     # unsupported layer shape, negative count
     assert f(FAKE, FAKE, 1, arr, arr, arr, arr, arr, 2048, 1024, eps, None) == 4
     assert f(FAKE, FAKE, -1, arr, arr, arr, arr, arr, 1024, 3584, eps, None) == 3
@@ -317,3 +323,33 @@ def test_measure_mma_s8_argument_errors(lib):
     assert lib.qg_measure_mma_s8((1 << 24) + 1, FAKE, ctypes.addressof(ops), None) == 3
     assert lib.qg_measure_mma_s8(10, None, ctypes.addressof(ops), None) == 1          # no sink
     assert lib.qg_measure_mma_s8(10, FAKE, None, None) == 1                           # nowhere to report
+
+
+def test_decode_stack_argument_errors(lib):
+    """qg_decode_stack_q8_0 refuses bad requests before anything is launched."""
+    f = lib.qg_decode_stack_q8_0
+    eps = ctypes.c_float(1e-6)
+    arr = (ctypes.c_void_p * 2)(FAKE, FAKE)
+    nul = (ctypes.c_void_p * 2)(FAKE, None)
+    mis = (ctypes.c_void_p * 2)(FAKE, FAKE + 16)  # a value plane 16- but not 32-byte aligned
+    assert lib.qg_decode_stack_max_layers() == 64
+    wsb = lib.qg_decode_stack_workspace_bytes(1024, 3584)
+    assert wsb > 256 + 8 * (1024 + 3584 // 4 + 3584 // 32)
+    assert lib.qg_decode_stack_workspace_bytes(2048, 3584) == -1  # hidden beyond one K block per lane group
+    assert lib.qg_decode_stack_workspace_bytes(1024, 4096 + 256) == -1
+    assert lib.qg_decode_stack_workspace_bytes(992, 3584) == -1  # hidden not a multiple of 256
+    X, Y, WS = FAKE, FAKE + (1 << 16), FAKE + (1 << 20)
+
+    def call(x=X, y=Y, n=2, g=arr, gq=arr, gd=arr, dq=arr, dd=arr, hidden=1024, ffn=3584, e=eps, ws=WS,
+             h=None, hq=None, hd=None, limit=0):
+        return f(x, y, n, g, gq, gd, dq, dd, hidden, ffn, e, ws, h, hq, hd, limit, None)
+
+    assert call(n=0) == 3 and call(n=65) == 3          # layer count
+    assert call(e=ctypes.c_float(-1.0)) == 3           # negative eps
+    assert call(limit=-5) == 3                         # negative wait limit
+    assert call(hidden=992) == 4 and call(ffn=3584 + 32) == 4 and call(hidden=2048) == 4
+    assert call(ws=None) == 1 and call(x=None) == 1 and call(gq=None) == 1 and call(dd=nul) == 1
+    assert call(ws=WS + 128) == 2 and call(x=X + 4) == 2 and call(gq=mis) == 2 and call(h=FAKE + 2) == 2
+    assert call(y=X + 64) == 3                         # output overlapping the input in part
+    assert call(y=WS + 4096) == 3                      # output inside the workspace
+    assert call(h=WS) == 3                             # h_last inside the workspace
