@@ -144,6 +144,49 @@ class ClockSampler:
                 "reasons": names, "samples": len(self.samples)}
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    import platform
+    import subprocess
+
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def gpu_processes():
+    """Compute processes on the GPUs as nvidia-smi lists them ("pid, name, memory"),
+    or None when the query is unavailable."""
+    import subprocess
+
+    try:
+        r = subprocess.run(["nvidia-smi", "--query-compute-apps=pid,process_name,used_memory", "--format=csv,noheader"],
+                           capture_output=True, text=True, timeout=20)
+    except (OSError, subprocess.SubprocessError):
+        return None
+    if r.returncode != 0:
+        return None
+    return [ln.strip() for ln in r.stdout.splitlines() if ln.strip()]
+
+
+def other_processes(procs):
+    if procs is None:
+        return None
+    me = str(os.getpid())
+    return [p for p in procs if p.split(",")[0].strip() != me]
+
+
 # --------------------------------------------------------------------------
 # distributed plumbing (one process per GPU; no collective on the data path)
 # --------------------------------------------------------------------------
@@ -282,37 +325,78 @@ def replicate_q8(torch, api, w0, copies: int):
     return [api.Q8Weight(qs[i], d[i]) for i in range(copies)]
 
 
-def extra_configs(torch, pk) -> dict:
-    """Kernel rates on the other workloads: cold (rotating copies >= 4x L2; median,
-    p10 and p90 of 20 timed replays) and, where the weights fit in L2, warm
-    (`us_warm_l2`, labelled as such)."""
-    import numpy as np
+def hbm_read_probe(torch) -> dict:
+    """The library's pure-read probe over a 2 GiB buffer (16x the L2): GB/s of
+    one read, median of 10 timed launches after 3 untimed."""
+    from block_quantized_decode_rmsnorm_gb300 import api
 
+    nbytes = 2 << 30
+    buf = torch.empty((nbytes,), dtype=torch.uint8, device="cuda")
+    buf.fill_(1)
+    sink = api.qg_measure_hbm_read(buf)
+    for _ in range(3):
+        api.qg_measure_hbm_read(buf, sink)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        api.qg_measure_hbm_read(buf, sink)
+        e1.record()
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) / 1e3)
+    del buf, sink
+    torch.cuda.empty_cache()
+    return {"GB/s": nbytes / statistics.median(ts) / 1e9, "bytes": nbytes,
+            "note": "qg_measure_hbm_read: every SM streams the buffer once with the GEMV kernels' 32-byte loads"}
+
+
+def config_summary(torch, pk, probe_gbs: float, variants: bool = False) -> tuple:
+    """One short entry per workload of the method besides the headline step:
+    per-launch time (median of 20 timed graph replays over rotating weight copies
+    >= 4x L2), the rate and its fraction of the measured peak (copy peak for HBM
+    work, and of the read probe; the measured bf16 dense peak for tensor work).
+    With `variants`, also every tile width and alternative kernel, returned
+    separately."""
     from block_quantized_decode_rmsnorm_gb300 import api, synth
 
-    out = {}
+    cfg, var = {}, {}
     hbm = pk["hbm_gbs"]
 
-    def gemv_rate(name, n, k, batch):
+    def hbm_entry(r, algo):
+        gbs = algo / (r["us"] / 1e6) / 1e9
+        e = {"us": round(r["us"], 3), "us_p90": round(r["us_p90"], 3), "GB/s": round(gbs, 1),
+             "frac_copy_peak": round(gbs / hbm, 4), "frac_read_probe": round(gbs / probe_gbs, 4)}
+        if "us_warm_l2" in r:
+            e["us_warm_l2"] = round(r["us_warm_l2"], 3)
+        return e
+
+    def gemv(n, k, batch):
         qs, d = synth.q8_0_weight_planes(0, synth.S_W0, n, k)
         w0 = api.q8_weight_from_numpy(qs, d)
-        wbytes = w0.nbytes
-        copies = l2_copies(torch, wbytes)
+        copies = l2_copies(torch, w0.nbytes)
         ws = replicate_q8(torch, api, w0, copies)
         x = torch.from_numpy(synth.f32_normal(0, synth.S_X, (batch, k))).cuda()
         xq, xd = api.quantize_act_q8_0(x)
         y = torch.empty((batch, n), dtype=torch.float32, device="cuda")
-        r = cold_and_warm(torch, lambda w: api.qgemv_q8_0(w, xq, xd, y=y), ws, wbytes)
-        algo = wbytes + batch * (k + (k // 32) * 2) + batch * n * 4
-        gbs = algo / (r["us"] / 1e6) / 1e9
-        out[name] = {**r, "GB/s": gbs, "frac_hbm": gbs / hbm, "bytes": algo}
+        r = cold_and_warm(torch, lambda w: api.qgemv_q8_0(w, xq, xd, y=y), ws, w0.nbytes)
+        algo = w0.nbytes + batch * (k + (k // 32) * 2) + batch * n * 4
         del ws
+        return r, algo, copies
 
-    gemv_rate("q8_0_gemv_256x1024_b1", 256, 1024, 1)
+    # 1: Q8_0 GEMV 256x1024, and an empty kernel chain of the same launch shape
+    r, algo, copies = gemv(256, 1024, 1)
+    e = hbm_entry(r, algo)
+    gf = capture(torch, lambda: api.qg_measure_launch_chain(copies, 32, 256))
+    e["launch_floor_us"] = round(replay_trials(torch, gf, copies)["median"] * 1e6, 3)
+    del gf
+    cfg["1_gemv_256x1024"] = e
+    # 4: output head 262144x1024, batch 1, 2, 4, 8
     for b in (1, 2, 4, 8):
-        gemv_rate(f"output_head_262144x1024_b{b}", 262144, 1024, b)
+        r, algo, _ = gemv(262144, 1024, b)
+        cfg[f"4_head_262144x1024_b{b}"] = hbm_entry(r, algo)
 
-    # bf16 projection with the norm fused in front, SiLU*u behind
+    # 3: bf16 gate|up 18432x2560, RMSNorm in front, SiLU*u behind
     bc = synth.bf16_case(0)
     w0 = api.bf16_from_bits(bc["w"])
     copies = l2_copies(torch, w0.numel() * 2)
@@ -321,29 +405,26 @@ def extra_configs(torch, pk) -> dict:
     yb = torch.empty((w0.shape[0] // 2,), dtype=torch.float32, device="cuda")
     r = cold_and_warm(torch, lambda w: api.qgemv_bf16(w, xb, gb, EPS, epilogue="silu_mul", y=yb), ws,
                       w0.numel() * 2)
-    algo = w0.numel() * 2 + 2 * 2 * w0.shape[1] + yb.numel() * 4
-    gbs = algo / (r["us"] / 1e6) / 1e9
-    out["bf16_proj_18432x2560_norm_silu"] = {**r, "GB/s": gbs, "frac_hbm": gbs / hbm, "bytes": algo}
+    cfg["3_bf16_18432x2560"] = hbm_entry(r, w0.numel() * 2 + 2 * 2 * w0.shape[1] + yb.numel() * 4)
 
-    # bf16 gate|up for a 512-row prompt on tcgen05: the whole call (row norms, then
-    # the projection with SiLU*u), and the projection alone on normalised rows
+    # next step 3: the same projection for a 512-row prompt on tcgen05 (row norms + projection)
     xp = api.bf16_from_bits(synth.bf16_normal_bits(0, synth.S_X + 7, (512, w0.shape[1])))
     xh = torch.empty_like(xp)
     yp16 = torch.empty((512, w0.shape[0] // 2), dtype=torch.float32, device="cuda")
     flops = 2 * 512 * w0.shape[0] * w0.shape[1]
-    for name, fn in (("prefill_bf16_512x18432x2560_norm_silu",
-                      lambda w: api.qgemm_bf16_prefill(w, xp, gb, EPS, epilogue="silu_mul", y=yp16, xhat=xh)),
-                     ("prefill_bf16_512x18432x2560_silu_gemm_only",
-                      lambda w: api.qgemm_bf16_prefill(w, xh, None, EPS, epilogue="silu_mul", y=yp16))):
+    bf16_fns = [("next3_prefill_bf16_512x18432x2560",
+                 lambda w: api.qgemm_bf16_prefill(w, xp, gb, EPS, epilogue="silu_mul", y=yp16, xhat=xh))]
+    if variants:
+        bf16_fns.append(("prefill_bf16_512x18432x2560_gemm_only",
+                         lambda w: api.qgemm_bf16_prefill(w, xh, None, EPS, epilogue="silu_mul", y=yp16)))
+    for i, (name, fn) in enumerate(bf16_fns):
         r = cold_and_warm(torch, fn, ws, w0.numel() * 2)
         tf = flops / (r["us"] / 1e6) / 1e12
-        out[name] = {**r, "TFLOP/s": tf, "frac_bf16_dense_peak": tf / pk["bf16_tflops"], "flops": flops}
+        (cfg if i == 0 else var)[name] = {"us": round(r["us"], 3), "TFLOP/s": round(tf, 1),
+                                          "frac_bf16_dense_peak": round(tf / pk["bf16_tflops"], 4)}
     del ws, xp, xh, yp16
 
-    # prompt-sized contraction: tensor-core path (activation tiles, tcgen05) at
-    # the library's tile width and at each fixed one, and the int8 mma.sync
-    # path, on the same rotating weight copies
-    # the int8 mma.sync path's rate, the prompt contraction's second roofline
+    # 5: prompt contraction 512x7168x1024 (wide tcgen05 tiles); int8 mma.sync rate as context
     api.qg_measure_mma_s8(100)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -352,49 +433,41 @@ def extra_configs(torch, pk) -> dict:
     e1.record()
     torch.cuda.synchronize()
     mma_tops = mops / (e0.elapsed_time(e1) / 1e3) / 1e12
-    out["mma_sync_s8_rate"] = {"TOPS": mma_tops, "int_ops": mops,
-                               "note": "independent m16n8k32 s8 MMAs on register operands, 4 CTAs per SM"}
-
     pc = synth.prefill_case(0)
     wp = api.q8_weight_from_numpy(pc["w_qs"], pc["w_d"])
     copies = l2_copies(torch, wp.nbytes)
     wps = replicate_q8(torch, api, wp, copies)
     xdev = torch.from_numpy(pc["x"]).cuda()
-    xq, xd = api.quantize_act_q8_0(xdev)
-    xt = api.quantize_act_q8_0_tiles(xdev)
     yp = torch.empty((512, 7168), dtype=torch.float32, device="cuda")
     ops = 2 * 512 * 7168 * 1024
-    variants = [("prefill_512x7168x1024_tcgen05", lambda w: api.qgemm_q8_0_prefill_tc(w, xt, y=yp))]
-    for bn in (64, 96, 128):
-        variants.append((f"prefill_512x7168x1024_tcgen05_bn{bn}",
-                         lambda w, bn=bn: api.qgemm_q8_0_prefill_tc(w, xt, y=yp, tile_n=bn)))
-    variants.append(("prefill_512x7168x1024_mma_sync", lambda w: api.qgemm_q8_0_prefill(w, xq, xd, y=yp)))
-    wbytes = {}
-    for name, _ in variants:
-        wbytes[name] = (wps, wp.nbytes)
-    # wide-tile form: weights packed once to binary16 codes + block-major scales
     wps2 = [api.qg_q8_0_pack_f16(w) for w in wps]
     x2 = api.quantize_act_q8_0_f16(xdev)
     w2bytes = wps2[0].codes.numel() * 2 + wps2[0].scales_t.numel() * 4
-    tc2 = [("prefill_512x7168x1024_tcgen05_wide", lambda w: api.qgemm_q8_0_prefill_tc2(w, x2, y=yp)),
-           ("prefill_512x7168x1024_tcgen05_wide_with_act_quant",
-            lambda w: api.qgemm_q8_0_prefill_tc2(w, api.quantize_act_q8_0_f16(xdev, out=x2), y=yp))]
-    for bn in (128, 192):
-        tc2.append((f"prefill_512x7168x1024_tcgen05_wide_bn{bn}",
-                    lambda w, bn=bn: api.qgemm_q8_0_prefill_tc2(w, x2, y=yp, tile_n=bn)))
-    for name, _ in tc2:
-        wbytes[name] = (wps2, w2bytes)
-    variants += tc2
-    for name, fn in variants:
-        ws_, nb_ = wbytes[name]
+    runs = [("5_prefill_512x7168x1024", lambda w: api.qgemm_q8_0_prefill_tc2(w, x2, y=yp), wps2, w2bytes, cfg)]
+    if variants:
+        xq, xd = api.quantize_act_q8_0(xdev)
+        xt = api.quantize_act_q8_0_tiles(xdev)
+        runs.append(("prefill_wide_with_act_quant",
+                     lambda w: api.qgemm_q8_0_prefill_tc2(w, api.quantize_act_q8_0_f16(xdev, out=x2), y=yp), wps2,
+                     w2bytes, var))
+        for bn in (128, 192):
+            runs.append((f"prefill_wide_bn{bn}", lambda w, bn=bn: api.qgemm_q8_0_prefill_tc2(w, x2, y=yp, tile_n=bn),
+                         wps2, w2bytes, var))
+        runs.append(("prefill_tile_records", lambda w: api.qgemm_q8_0_prefill_tc(w, xt, y=yp), wps, wp.nbytes, var))
+        for bn in (64, 96, 128):
+            runs.append((f"prefill_tile_records_bn{bn}",
+                         lambda w, bn=bn: api.qgemm_q8_0_prefill_tc(w, xt, y=yp, tile_n=bn), wps, wp.nbytes, var))
+        runs.append(("prefill_mma_sync", lambda w: api.qgemm_q8_0_prefill(w, xq, xd, y=yp), wps, wp.nbytes, var))
+    for name, fn, ws_, nb_, dst in runs:
         r = cold_and_warm(torch, fn, ws_, nb_)
         tops = ops / (r["us"] / 1e6) / 1e12
-        out[name] = {**r, "TOPS": tops, "frac_f16_dense_peak": tops / pk["bf16_tflops"],
-                     "frac_mma_s8_rate": tops / mma_tops, "int_ops": ops}
+        dst[name] = {"us": round(r["us"], 3), "TOPS": round(tops, 1),
+                     "frac_f16_dense_peak": round(tops / pk["bf16_tflops"], 4),
+                     "x_mma_s8_rate": round(tops / mma_tops, 3)}
+    cfg["5_prefill_512x7168x1024"]["mma_s8_rate_tops"] = round(mma_tops, 1)
     del wps, wps2
     torch.cuda.empty_cache()
-    _ = np
-    return out
+    return cfg, var
 
 
 def ncu_traffic(kernel_key: str):
@@ -445,7 +518,7 @@ def cpu_baseline(seconds: float, n_layers: int, all_cores: bool = True) -> dict:
     time budget is spent, on one host thread; and the same loop in one process
     per host core (spawned, so no GPU state is inherited), summed."""
     done, el = _oracle_layers((seconds, n_layers))
-    out = {"value": done * LAYER_BYTES / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+    out = {"value": done * LAYER_BYTES / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle", "cpu_model": cpu_model(),
            "sample": f"{done} FFN layers (hidden {HIDDEN}, ffn {FFN}) of the {n_layers}-layer step in {el:.1f} s, "
                      "plain C oracle, one host thread"}
     if all_cores:
@@ -512,6 +585,7 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     sampler = ClockSampler(torch, dev)
+    procs_before = other_processes(gpu_processes())
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     dist.barrier()
     torch.cuda.synchronize()
@@ -522,6 +596,7 @@ def run_ours(args):
     e1.record()
     torch.cuda.synchronize()
     clocks = sampler.stop()
+    procs_after = other_processes(gpu_processes())
     dist.barrier()
     elapsed = dist.max(e0.elapsed_time(e1) / 1e3)
     step_bytes = L * LAYER_BYTES
@@ -609,9 +684,16 @@ def run_ours(args):
                             "four": "four launches per layer (decode_ffn_q8_0)"}[path],
                    "parallelism": f"replicas x{dist.world} (independent decode streams, no collective)"},
         "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
+        "other_gpu_processes": {"before": procs_before, "after": procs_after},
     }
     if not args.quick:
-        line["other_workloads"] = extra_configs(torch, pk)
+        probe = hbm_read_probe(torch)
+        cfgs, var = config_summary(torch, pk, probe["GB/s"], args.variants)
+        line["hbm_read_probe"] = {"GB/s": round(probe["GB/s"], 1), "frac_copy_peak": round(probe["GB/s"] / pk["hbm_gbs"], 4)}
+        line["roofline"]["frac_read_probe"] = line["roofline"]["achieved"] / probe["GB/s"]
+        line["configs"] = cfgs
+        if var:
+            line["variants"] = var
     if dist.rank == 0 and dist.world == 1:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds, L)
     if dist.rank == 0:
@@ -720,7 +802,8 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": workload_name(L), "layers": L, "batch": 1, "layers_per_step_sampled": per_step},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
+                         "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
@@ -733,6 +816,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layers", type=int, default=24)
     ap.add_argument("--quick", action="store_true", help="skip the other workloads' kernel rates")
+    ap.add_argument("--variants", action="store_true",
+                    help="also time every tile width and alternative kernel of the other workloads")
     ap.add_argument("--path", choices=["stack", "one", "two", "four"], default="two",
                     help="stack: every layer in one persistent launch; otherwise launches per decode layer: one "
                          "(split-K down inside the layer kernel), two, four")

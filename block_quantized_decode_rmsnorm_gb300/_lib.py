@@ -49,6 +49,9 @@ SIGNATURES = {
     "qg_decode_stack_q8_0": (ST, [P, P, I32, P, P, P, P, P, I64, I64, F32, P, P, P, P, I64, P]),
     "qg_debug_block_dots_q8_0": (ST, [P, I64, I64, P, I64, P, P]),
     "qg_measure_mma_s8": (ST, [I64, P, P, P]),
+    "qg_measure_hbm_read_sink_len": (I32, []),
+    "qg_measure_hbm_read": (ST, [P, I64, P, I32, P]),
+    "qg_measure_launch_chain": (ST, [I32, I32, I32, P]),
     "qg_scales_ld": (I64, [I64]),
     "qg_q8_0_pack_f16": (ST, [P, P, I64, I64, P, P, P]),
     "quantize_act_q8_0_f16": (ST, [P, I64, I64, P, P, P]),

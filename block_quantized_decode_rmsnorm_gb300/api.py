@@ -351,6 +351,22 @@ def qg_measure_mma_s8(iters: int, stream=None) -> int:
     return ops.value
 
 
+def qg_measure_hbm_read(buf: torch.Tensor, sink: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """One streaming read of the whole device buffer `buf` (the pure-read probe);
+    returns the per-CTA fold words so that the caller can keep them alive."""
+    n = _lib.load().qg_measure_hbm_read_sink_len()
+    if sink is None:
+        sink = torch.empty((n,), dtype=torch.int32, device=buf.device)
+    _lib.call("qg_measure_hbm_read", buf.data_ptr(), buf.numel() * buf.element_size(), sink.data_ptr(), sink.numel(),
+              _stream_handle(stream))
+    return sink
+
+
+def qg_measure_launch_chain(n: int, grid: int, block: int, stream=None) -> None:
+    """n empty kernels with programmatic dependent launch (the launch floor)."""
+    _lib.call("qg_measure_launch_chain", n, grid, block, _stream_handle(stream))
+
+
 def qg_debug_block_dots_q8_0(w: Q8Weight, xq: torch.Tensor, s: torch.Tensor | None = None,
                              stream=None) -> torch.Tensor:
     """Exact int32 block sums s[batch, n_rows, k/32]."""

@@ -40,6 +40,9 @@ cudaError_t launch_quantize_act_tiles(const float *, int64_t, int64_t, void *, c
 bool prefill_tc_supported(int64_t k);
 bool prefill_bf16_supported(int64_t k);
 cudaError_t launch_mma_s8_rate(int64_t, int *, int64_t *, cudaStream_t);
+int hbm_read_ctas();
+cudaError_t launch_hbm_read(const void *, int64_t, uint32_t *, cudaStream_t);
+cudaError_t launch_empty_chain(int, int, int, cudaStream_t);
 cudaError_t launch_pack_q8_0_f16(const int8_t *, const uint16_t *, int64_t, int64_t, uint16_t *, float *, cudaStream_t);
 cudaError_t launch_quantize_act_f16(const float *, int64_t, int64_t, uint16_t *, float *, cudaStream_t);
 cudaError_t launch_prefill_tc2(const uint16_t *, const float *, int64_t, int64_t, const uint16_t *, const float *,
@@ -528,6 +531,24 @@ qg_status qg_measure_mma_s8(int64_t iters, int32_t *sink, int64_t *ops, qg_strea
     if (iters < 1 || iters > (int64_t(1) << 24)) return QG_ERR_SHAPE;
     if (!sink || !ops) return QG_ERR_NULL;
     return from_cuda(qg::launch_mma_s8_rate(iters, sink, ops, stream));
+}
+
+int32_t qg_measure_hbm_read_sink_len(void) { return qg::hbm_read_ctas(); }
+
+qg_status qg_measure_hbm_read(const void *buf, int64_t bytes, uint32_t *sink, int32_t sink_len, qg_stream_t stream)
+{
+    if (bytes <= 0 || bytes % 32 != 0) return QG_ERR_SHAPE;
+    if (!buf || !sink) return QG_ERR_NULL;
+    if (!aligned(buf, 32) || !aligned(sink, 4)) return QG_ERR_ALIGN;
+    if (sink_len < qg::hbm_read_ctas()) return QG_ERR_SHAPE;
+    return from_cuda(qg::launch_hbm_read(buf, bytes, sink, stream));
+}
+
+qg_status qg_measure_launch_chain(int32_t n, int32_t grid, int32_t block, qg_stream_t stream)
+{
+    if (n < 0 || n > 65536 || grid < 1 || grid > 65535 || block < 1 || block > 1024 || block % 32 != 0)
+        return QG_ERR_SHAPE;
+    return from_cuda(qg::launch_empty_chain(n, grid, block, stream));
 }
 
 qg_status qg_debug_block_dots_q8_0(const int8_t *w_qs, int64_t n_rows, int64_t k, const int8_t *xq, int64_t batch,

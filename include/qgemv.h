@@ -481,6 +481,31 @@ QG_API qg_status qgemm_q8_0_prefill_tc2(const uint16_t *w_codes, const float *w_
 QG_API qg_status qg_measure_mma_s8(int64_t iters, int32_t *sink, int64_t *ops, qg_stream_t stream);
 
 /*
+ * qg_measure_hbm_read - reads `bytes` of device memory once, from every SM, with
+ * the 32-byte streaming loads of the GEMV kernels, and folds them into one word
+ * per CTA of `sink`: the pure-read bandwidth probe that a decode product is
+ * judged against ([Herbert] Decode: memory decides: decode matvec against a
+ * pure-read probe on the same machine).  A caller times the stream.
+ *   buf: device, 32-byte aligned; bytes: a positive multiple of 32;
+ *   sink: device uint32[sink_len], sink_len >= qg_measure_hbm_read_sink_len().
+ *   Errors: QG_ERR_SHAPE, QG_ERR_NULL, QG_ERR_ALIGN, QG_ERR_CUDA.
+ */
+QG_API int32_t qg_measure_hbm_read_sink_len(void);
+QG_API qg_status qg_measure_hbm_read(const void *buf, int64_t bytes, uint32_t *sink, int32_t sink_len,
+                                     qg_stream_t stream);
+
+/*
+ * qg_measure_launch_chain - launches n empty kernels of grid x block threads on
+ * `stream`, each waiting for its predecessor and letting its successor launch
+ * (programmatic dependent launch, as every kernel of the library): timed by the
+ * caller, the cost of a kernel boundary alone, the floor of a GEMV whose bytes
+ * take less time than its launch.  Not part of the method.
+ *   n: 0 .. 65536; grid: 1 .. 65535; block: a multiple of 32 up to 1024.
+ *   Errors: QG_ERR_SHAPE, QG_ERR_CUDA.
+ */
+QG_API qg_status qg_measure_launch_chain(int32_t n, int32_t grid, int32_t block, qg_stream_t stream);
+
+/*
  * qgemm_bf16_prefill - qgemv_bf16 for m prompt rows at once, on the tcgen05
  * tensor cores ([Herbert] The numerical contract: bf16 weights and activations,
  * f32 accumulators; Emitting for a GPU: norm fused in front, SiLU(g)*u behind,
