@@ -70,6 +70,7 @@ def _load():
                 "orc_silu_mul": (None, [P, P, I64, P]),
                 "orc_gemv_bf16": (None, [P, I64, I64, P, P, F, P, P, P, P]),
                 "orc_residual_add": (None, [P, P, I64, P]),
+                "orc_hadamard128": (None, [P, I64, P]),
                 "orc_decode_ffn": (None, [P, P, I64, I64, F, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P]),
             }
             for name, (res, args) in sig.items():
@@ -231,6 +232,27 @@ def gemv_bf16(w_bits, x_bits, gamma_bits, eps: float):
 # --------------------------------------------------------------------------
 # composite steps, in the pages' order
 # --------------------------------------------------------------------------
+
+def hadamard128(x) -> np.ndarray:
+    """z f64[n]: the order-128 Walsh-Hadamard transform (Sylvester order,
+    unnormalised) of each consecutive block of 128 values of x (f32)."""
+    lib = _load()
+    x = _c(x, np.float32).ravel()
+    if x.size % 128:
+        raise ValueError("n must be a multiple of 128")
+    z = np.empty(x.size, np.float64)
+    lib.orc_hadamard128(_ptr(x), x.size, _ptr(z))
+    return z
+
+
+def rmsnorm_hadamard(x, gamma, eps: float):
+    """x_hat = (x * r) * gamma (orc_rmsnorm_quantize's), then its rotation z
+    (f64) and the magnitude sum a of the 128 terms of each z value."""
+    _, _, r, xh = rmsnorm_quantize(x, gamma, eps)
+    z = hadamard128(xh)
+    a = np.repeat(np.abs(xh.astype(np.float64)).reshape(-1, 128).sum(1), 128)
+    return z, a, r, xh
+
 
 def residual_add(res, y) -> np.ndarray:
     """out f64[n] = res (f32) + y (f64)."""

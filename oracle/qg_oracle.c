@@ -327,6 +327,34 @@ void orc_silu_mul(const double *g, const double *u, int64_t n, double *h)
         h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];
 }
 
+/* Rotation of the normalised activation ([Phobos] PrismML Ternary-Bonsai-2-27B:
+ * the format applies a Hadamard matrix transform to the activation, which
+ * spreads outliers over the block, and the rotated activation is computed once
+ * and shared by every projection that reads the same input).  Reading: the
+ * Walsh-Hadamard matrix of order 128 (the format's block of 128 weights) in
+ * Sylvester order, unnormalised (entries +1 / -1, H H^T = 128 I), applied to
+ * each consecutive block of 128 values:
+ *   z[128 b + i] = sum_j (-1)^popcount(i & j) x[128 b + j],
+ * evaluated term by term in f64 from the definition (n a multiple of 128). */
+void orc_hadamard128(const float *x, int64_t n, double *z)
+{
+    for (int64_t b = 0; b < n / 128; ++b) {
+        for (int i = 0; i < 128; ++i) {
+            double sum = 0.0;
+            for (int j = 0; j < 128; ++j) {
+                int bits = i & j, par = 0;
+                while (bits) {
+                    par ^= bits & 1;
+                    bits >>= 1;
+                }
+                const double v = (double)x[128 * b + j];
+                sum += par ? -v : v;
+            }
+            z[128 * b + i] = sum;
+        }
+    }
+}
+
 /* Residual folded into the last product ([Phobos] Fast Decode): out[n] =
  * res[n] + y[n] in f64 (res is f32, so exact in f64; y is the exact f64 value of
  * the block-scaled sum). */
