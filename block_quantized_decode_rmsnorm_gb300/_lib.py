@@ -32,6 +32,7 @@ SIGNATURES = {
     "qg_act_tiles_bytes": (I64, [I64, I64]),
     "quantize_act_q8_0_tiles": (ST, [P, I64, I64, P, P]),
     "rmsnorm_quantize": (ST, [P, P, I64, I64, F32, P, P, P, P]),
+    "rmsnorm_hadamard_quantize": (ST, [P, P, I64, I64, F32, P, P, P, P, P]),
     "qgemv_q8_0": (ST, [P, P, I64, I64, P, P, I64, I32, P, P, P]),
     "qgemv_bf16": (ST, [P, I64, I64, P, P, F32, I32, P, P, P]),
     "qgemm_q8_0_prefill": (ST, [P, P, I64, I64, P, P, I64, P, P]),

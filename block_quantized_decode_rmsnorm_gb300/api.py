@@ -163,6 +163,29 @@ def rmsnorm_quantize(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6, q=
     return q, d, inv_rms
 
 
+def rmsnorm_hadamard_quantize(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6, q=None, d=None, z=None,
+                              inv_rms=None, stream=None):
+    """Per row: x_hat = RMSNorm(x) * gamma, rotated by the order-128 Walsh-Hadamard
+    transform on each block of 128, then Q8_0 -> (q int8[rows][k], d f16[rows][k/32])."""
+    x2 = _as_2d(x)
+    rows, k = x2.shape
+    _need(x2, "x", torch.float32)
+    _need(gamma, "gamma", torch.float32, (k,))
+    if q is None:
+        q = torch.empty((rows, k), dtype=torch.int8, device=x.device)
+    if d is None:
+        d = torch.empty((rows, k // 32), dtype=torch.float16, device=x.device)
+    _need(q, "q", torch.int8, (rows, k))
+    _need(d, "d", torch.float16, (rows, k // 32))
+    if z is not None:
+        _need(z, "z", torch.float32, (rows, k))
+    if inv_rms is not None:
+        _need(inv_rms, "inv_rms", torch.float32, (rows,))
+    _lib.call("rmsnorm_hadamard_quantize", x2.data_ptr(), gamma.data_ptr(), rows, k, float(eps), q.data_ptr(),
+              d.data_ptr(), _ptr(z), _ptr(inv_rms), _stream_handle(stream))
+    return q, d
+
+
 def qgemv_q8_0(w: Q8Weight, xq: torch.Tensor, xd: torch.Tensor, epilogue: str | int = "none",
                residual: torch.Tensor | None = None, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Block-scaled Q8_0 GEMV; y f32 [batch, n_out]."""
@@ -433,6 +456,29 @@ def decode_ffn_q8_0(x: torch.Tensor, layer: FFNLayer, buf: FFNBuffers, eps: floa
     ffn = layer.down.k
     _lib.call("rmsnorm_quantize", x.data_ptr(), layer.gamma.data_ptr(), 1, hidden, float(eps), buf.xq.data_ptr(),
               buf.xd.data_ptr(), None, s)
+    _lib.call("qgemv_q8_0", layer.gate_up.qs.data_ptr(), layer.gate_up.d.data_ptr(), 2 * ffn, hidden,
+              buf.xq.data_ptr(), buf.xd.data_ptr(), 1, QG_EPI_SILU_MUL_HALVES, None, buf.h.data_ptr(), s)
+    _lib.call("quantize_act_q8_0", buf.h.data_ptr(), 1, ffn, buf.hq.data_ptr(), buf.hd.data_ptr(), s)
+    _lib.call("qgemv_q8_0", layer.down.qs.data_ptr(), layer.down.d.data_ptr(), hidden, ffn, buf.hq.data_ptr(),
+              buf.hd.data_ptr(), 1, QG_EPI_RESIDUAL_ADD, x.data_ptr(), x.data_ptr(), s)
+
+
+def decode_ffn_q8_0_rotated(x: torch.Tensor, layer: FFNLayer, buf: FFNBuffers, eps: float = 1e-6,
+                            stream=None) -> None:
+    """decode_ffn_q8_0 with the normalised activation rotated once (order-128
+    Walsh-Hadamard per block) before it is quantized; the stacked gate|up weights
+    of `layer` are the rotated ones (W H^T / 128, quantized at load time), so both
+    halves read the one rotated activation.
+
+    "Filling in the blanks: Inference using Phobos", PrismML Ternary-Bonsai-2-27B:
+    the rotated activation is computed once and shared by every projection that
+    reads the same input.
+    """
+    s = _stream_handle(stream)
+    hidden = x.shape[-1]
+    ffn = layer.down.k
+    _lib.call("rmsnorm_hadamard_quantize", x.data_ptr(), layer.gamma.data_ptr(), 1, hidden, float(eps),
+              buf.xq.data_ptr(), buf.xd.data_ptr(), None, None, s)
     _lib.call("qgemv_q8_0", layer.gate_up.qs.data_ptr(), layer.gate_up.d.data_ptr(), 2 * ffn, hidden,
               buf.xq.data_ptr(), buf.xd.data_ptr(), 1, QG_EPI_SILU_MUL_HALVES, None, buf.h.data_ptr(), s)
     _lib.call("quantize_act_q8_0", buf.h.data_ptr(), 1, ffn, buf.hq.data_ptr(), buf.hd.data_ptr(), s)

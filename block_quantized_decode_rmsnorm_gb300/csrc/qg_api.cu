@@ -11,6 +11,8 @@ cudaError_t launch_quantize_act(const float *, int64_t, int64_t, int8_t *, uint1
 cudaError_t launch_rmsnorm_quantize(const float *, const float *, int64_t, int64_t, float, int8_t *, uint16_t *,
                                     float *, cudaStream_t);
 cudaError_t launch_pack_q8_0(const void *, int64_t, int64_t, int8_t *, uint16_t *, cudaStream_t);
+cudaError_t launch_rmsnorm_hadamard_quantize(const float *, const float *, int64_t, int64_t, float, int8_t *,
+                                             uint16_t *, float *, float *, cudaStream_t);
 cudaError_t launch_column_blocks(const int8_t *, const uint16_t *, int64_t, int64_t, int8_t *, uint16_t *,
                                  cudaStream_t);
 cudaError_t launch_gemv_q8_0(const int8_t *, const uint16_t *, int64_t, int64_t, const int8_t *, const uint16_t *,
@@ -213,6 +215,20 @@ qg_status rmsnorm_quantize(const float *x, const float *gamma, int64_t rows, int
     if (!aligned(x, 16) || !aligned(gamma, 16) || !aligned(q, 16) || !aligned(d, 2) || !aligned(inv_rms, 4))
         return QG_ERR_ALIGN;
     return from_cuda(qg::launch_rmsnorm_quantize(x, gamma, rows, k, eps, q, d, inv_rms, stream));
+}
+
+qg_status rmsnorm_hadamard_quantize(const float *x, const float *gamma, int64_t rows, int64_t k, float eps,
+                                    int8_t *q, uint16_t *d, float *z, float *inv_rms, qg_stream_t stream)
+{
+    if (rows < 0 || rows > (int64_t(1) << 31) - 1) return QG_ERR_SHAPE;
+    if (k <= 0 || k % 128 != 0 || k > 65536) return QG_ERR_SHAPE;
+    if (!(eps >= 0.0f)) return QG_ERR_SHAPE;
+    if (rows == 0) return QG_OK;
+    if (!x || !gamma || !q || !d) return QG_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(gamma, 16) || !aligned(q, 16) || !aligned(d, 2) || !aligned(z, 16) ||
+        !aligned(inv_rms, 4))
+        return QG_ERR_ALIGN;
+    return from_cuda(qg::launch_rmsnorm_hadamard_quantize(x, gamma, rows, k, eps, q, d, z, inv_rms, stream));
 }
 
 qg_status qgemv_q8_0(const int8_t *w_qs, const uint16_t *w_d, int64_t n_rows, int64_t k, const int8_t *xq,

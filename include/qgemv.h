@@ -167,6 +167,28 @@ QG_API qg_status rmsnorm_quantize(const float *x, const float *gamma, int64_t ro
                            qg_stream_t stream);
 
 /*
+ * rmsnorm_hadamard_quantize - rmsnorm_quantize with the normalised row rotated
+ * before it is quantized ([Phobos] PrismML Ternary-Bonsai-2-27B: a Hadamard
+ * matrix transform rotates the activation over the format's block, spreading
+ * outliers over it; the rotated activation is computed once and shared by every
+ * projection that reads the same input, whose weights carry the inverse
+ * rotation from load time: W x_hat = (W H^T / 128)(H x_hat)).  Per row:
+ *   r, x_hat = (x * r) * gamma            exactly as rmsnorm_quantize
+ *   z[128 b + i] = sum_j (-1)^popcount(i & j) x_hat[128 b + j]
+ *       (Walsh-Hadamard matrix of order 128, Sylvester order, unnormalised,
+ *        on each block of 128; summed in f32 by the fast transform's
+ *        butterflies, strides 1, 2, 4, ..., 64 in that order)
+ *   q, d   = Q8_0(z)                        (as quantize_act_q8_0 of z)
+ *   x, gamma: f32[rows][k] / f32[k], 16-byte aligned; k a multiple of 128 up to
+ *   65536; q: int8[rows][k] (16-byte aligned); d: binary16[rows][k/32];
+ *   z: optional f32[rows][k] (16-byte aligned) receiving the rotated row;
+ *   inv_rms: optional f32[rows].  Errors as rmsnorm_quantize.
+ */
+QG_API qg_status rmsnorm_hadamard_quantize(const float *x, const float *gamma, int64_t rows, int64_t k,
+                                           float eps, int8_t *q_out, uint16_t *d_out, float *z_out,
+                                           float *inv_rms_out, qg_stream_t stream);
+
+/*
  * qgemv_q8_0 - block-scaled Q8_0 matrix-vector product ([Phobos] Fast Decode:
  * int8 dot products end to end, one scale per 32 values, a warp owns an output
  * row and reduces with shuffles).

@@ -72,3 +72,21 @@ def test_rotation_preserves_the_product(orc):
     yr = (W @ Hb.T / 128.0) @ z
     assert np.max(np.abs(y - yr)) < 1e-12 * np.max(np.abs(W) @ np.abs(xh))
     assert np.all(a >= np.abs(z))
+
+
+def test_rotation_spreads_an_outlier(orc):
+    """The purpose the pages give the rotation: with one large value in a block,
+    Q8_0 of the rotated block loses less (relative to the block's norm, which the
+    rotation preserves up to the factor sqrt(128)) than Q8_0 of the block itself."""
+    x = synth.f32_normal(0, 99, (1024,))
+    x[200] = 60.0
+    x[777] = -45.0
+    gamma = np.ones(1024, np.float32)
+    z, _, _, xh = orc.rmsnorm_hadamard(x, gamma, 1e-6)
+
+    def rel_err(v):
+        q, d = orc.quantize_q8_0(v.astype(np.float32)[None, :])
+        deq = q[0].astype(np.float64) * np.repeat(orc.f16_bits_to_f64(d[0]), 32)
+        return np.linalg.norm(deq - v) / np.linalg.norm(v)
+
+    assert rel_err(z) < 0.5 * rel_err(xh.astype(np.float64))
