@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
         if (live) {
             const float dd = div127(m);
-            xc = q8_pack4(v, dd, __frcp_rn(dd));
+            xc = q8_pack4(v, dd, q8_recip(dd));
             const uint16_t dbits = f2h_rn(dd);
             xdf = h2f(dbits);
             if (blockIdx.x == 0) {
@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
         p.h[ob + lane] = v;
         const float m = warp_max_abs(v);
         const float dd = div127(m);
-        const int8_t code = static_cast<int8_t>(q8_code(v, dd, __frcp_rn(dd)));
+        const int8_t code = static_cast<int8_t>(q8_code(v, dd, q8_recip(dd)));
         const uint16_t dbits = f2h_rn(dd);
         p.hq[ob + lane] = code;
         if (lane == 0) p.hd[blockIdx.x] = dbits;

@@ -80,7 +80,7 @@ __global__ void quantize_act_f16_kernel(const float *x, int64_t m, int k, uint16
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
     if (!live) return;
     const float dd = div127(mx);
-    const float rd = __frcp_rn(dd);
+    const float rd = q8_recip(dd);
     const float q[4] = {static_cast<float>(q8_code(v.x, dd, rd)), static_cast<float>(q8_code(v.y, dd, rd)),
                         static_cast<float>(q8_code(v.z, dd, rd)), static_cast<float>(q8_code(v.w, dd, rd))};
     uint32_t h[2];

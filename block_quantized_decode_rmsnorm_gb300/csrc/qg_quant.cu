@@ -28,7 +28,7 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restri
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
     if (!live) return;
     const float dd = div127(m);
-    const float rd = __frcp_rn(dd);
+    const float rd = q8_recip(dd);
     reinterpret_cast<uint32_t *>(q + blk * QK)[sub] = q8_pack4(v, dd, rd);
     if (sub == 0) d[blk] = f2h_rn(dd);
 }
@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(256) quantize_act_tiles_kernel(const float *__
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
     const float dd = div127(m);
-    const float rd = __frcp_rn(dd);
+    const float rd = q8_recip(dd);
     const uint32_t c0 = __half_as_ushort(__int2half_rn(q8_code(v.x, dd, rd)));
     const uint32_t c1 = __half_as_ushort(__int2half_rn(q8_code(v.y, dd, rd)));
     const uint32_t c2 = __half_as_ushort(__int2half_rn(q8_code(v.z, dd, rd)));
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_quantize_kernel(
         if (live) {
             const float dd = div127(m);
             int8_t *qb = q + static_cast<int64_t>(row) * k + b * QK;
-            reinterpret_cast<uint32_t *>(qb)[sub] = q8_pack4(v, dd, __frcp_rn(dd));
+            reinterpret_cast<uint32_t *>(qb)[sub] = q8_pack4(v, dd, q8_recip(dd));
             if (sub == 0) d[static_cast<int64_t>(row) * nb + b] = f2h_rn(dd);
         }
     }

@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(ROT_THREADS) rmsnorm_hadamard_quantize_kernel(
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         const float dd = div127(mx);
-        *reinterpret_cast<uint32_t *>(q + static_cast<int64_t>(row) * k + o) = q8_pack4(zv, dd, __frcp_rn(dd));
+        *reinterpret_cast<uint32_t *>(q + static_cast<int64_t>(row) * k + o) = q8_pack4(zv, dd, q8_recip(dd));
         if ((lane & 7) == 0) d[static_cast<int64_t>(row) * nb + 4 * c + (lane >> 3)] = f2h_rn(dd);
     }
 }

@@ -401,7 +401,7 @@ __global__ void __launch_bounds__(kStackThreads, 1) decode_stack_kernel(const __
                 m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
                 if (live) {
                     const float dd = div127(m);
-                    xc = q8_pack4(v, dd, __frcp_rn(dd));
+                    xc = q8_pack4(v, dd, q8_recip(dd));
                     xdf = h2f(f2h_rn(dd));
                 }
             }
@@ -455,7 +455,7 @@ __global__ void __launch_bounds__(kStackThreads, 1) decode_stack_kernel(const __
                 const float v = silu_mul(row_total(0), row_total(1));
                 const float m = warp_max_abs(v);
                 const float dd = div127(m);
-                const uint32_t code = static_cast<uint32_t>(q8_code(v, dd, __frcp_rn(dd))) & 0xffu;
+                const uint32_t code = static_cast<uint32_t>(q8_code(v, dd, q8_recip(dd))) & 0xffu;
                 const uint16_t dbits = f2h_rn(dd);
                 // lane j holds code word j % 8 and writes it to copies j / 8 + 4 m;
                 // lanes below kStackReplicas write the scale word's copies
