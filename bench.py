@@ -622,6 +622,15 @@ def run_ours(args):
         del gu_graph
         kbytes, kname, kkey = GU_KERNEL_BYTES, "ffn_up_kernel<1> (RMSNorm + Q8_0 + gate|up 7168x1024 + SiLU*u + Q8_0)", \
             "ffn_up_kernel"
+    # the floor's measured inputs: an empty kernel chain of the step's launch count
+    # and launch shape (one CTA per SM), and the step's bytes at the measured peaks
+    n_chain = max(2, launches_per_step)
+    g_floor = capture(torch, lambda: api.qg_measure_launch_chain(n_chain, min(152, torch.cuda.get_device_properties(
+        dev).multi_processor_count), 256))
+    edge_us = replay_trials(torch, g_floor, n_chain)["median"] * 1e6
+    del g_floor
+    floor = {"empty_launch_us": round(edge_us, 3), "launches_per_step": launches_per_step,
+             "hbm_us_per_step_copy_peak": round(L * LAYER_BYTES / pk["hbm_gbs"] / 1e3, 2)}
     achieved = kbytes / t_k / 1e9
     roofline = {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / pk["hbm_gbs"], "peak_source": pk["source"], "algorithmic_bytes_per_launch": kbytes,
@@ -684,13 +693,14 @@ def run_ours(args):
                             "four": "four launches per layer (decode_ffn_q8_0)"}[path],
                    "parallelism": f"replicas x{dist.world} (independent decode streams, no collective)"},
         "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
-        "other_gpu_processes": {"before": procs_before, "after": procs_after},
+        "other_gpu_processes": {"before": procs_before, "after": procs_after}, "step_floor_inputs": floor,
     }
     if not args.quick:
         probe = hbm_read_probe(torch)
         cfgs, var = config_summary(torch, pk, probe["GB/s"], args.variants)
         line["hbm_read_probe"] = {"GB/s": round(probe["GB/s"], 1), "frac_copy_peak": round(probe["GB/s"] / pk["hbm_gbs"], 4)}
         line["roofline"]["frac_read_probe"] = line["roofline"]["achieved"] / probe["GB/s"]
+        floor["hbm_us_per_step_read_probe"] = round(L * LAYER_BYTES / probe["GB/s"] / 1e3, 2)
         line["configs"] = cfgs
         if var:
             line["variants"] = var

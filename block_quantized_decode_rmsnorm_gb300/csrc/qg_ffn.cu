@@ -259,8 +259,9 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
         if constexpr (!DOWN) return;
     }
     if (staged) {
-    f32pair tot = {0.0f, 0.0f};
-    if (lane < NW) tot = f32pair{s_part[2 * lane], s_part[2 * lane + 1]};
+    // every group of NW lanes merges the NW warp partials in one xor butterfly;
+    // pair_merge is exactly commutative, so every lane ends with the same total
+    f32pair tot = f32pair{s_part[2 * (lane % NW)], s_part[2 * (lane % NW) + 1]};
     float4 g4 = make_float4(0.f, 0.f, 0.f, 0.f);
     if (live) g4 = *reinterpret_cast<const float4 *>(s_gamma + xo);
 #pragma unroll
@@ -270,8 +271,6 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
         o.lo = __shfl_xor_sync(0xffffffffu, tot.lo, off);
         tot = pair_merge(tot, o);
     }
-    tot.hi = __shfl_sync(0xffffffffu, tot.hi, 0);
-    tot.lo = __shfl_sync(0xffffffffu, tot.lo, 0);
     const float r = rms_inv_from_pair(tot, K, p.inv_k, p.eps);
 
     // ---- Q8_0 quantization of x_hat = (x * r) * gamma, eight threads per block
