@@ -99,3 +99,69 @@ def test_pack_matches_oracle(torch, orc):
     oq, od = orc.q8_0_pack(blocks, 129, 1024)
     assert np.array_equal(w.qs.cpu().numpy(), oq)
     assert np.array_equal(f16_to_np_bits(w.d), od)
+
+
+def _near_midpoint_row(offset_rel):
+    """x (f32[1024]) with eps = 0 whose exact r = 1/sqrt(mean(x^2)) is
+    r_mid * (1 + offset_rel), r_mid = 1 + 2^-24 the midpoint between f32 1.0 and
+    its successor: 1020 ones and four values chosen greedily (each the largest
+    f32 whose square fits the remainder) so that the sum of squares S matches
+    1024 / r^2 to about 2^-80.  Exact rational arithmetic throughout.
+    Returns x, S and the target sum T."""
+    from fractions import Fraction as Fr
+
+    r_t = (1 + Fr(1, 2 ** 24)) * (1 + Fr(offset_rel))
+    T = Fr(1024) / (r_t * r_t)
+    rem = T - 1020
+
+    def f32_below_sqrt(v):
+        f = np.float32(float(v) ** 0.5)
+        while Fr(float(f)) ** 2 > v:
+            f = np.nextafter(f, np.float32(0))
+        while Fr(float(np.nextafter(f, np.float32(np.inf)))) ** 2 <= v:
+            f = np.nextafter(f, np.float32(np.inf))
+        return f
+
+    vals = [np.float32(1.0)] * 1020
+    a = f32_below_sqrt(rem - 1)
+    vals.append(a)
+    rem -= Fr(float(a)) ** 2
+    vals.append(np.float32(1.0))
+    rem -= 1
+    for _ in range(2):
+        b = f32_below_sqrt(rem)
+        vals.append(b)
+        rem -= Fr(float(b)) ** 2
+    x = np.array(vals, np.float32)
+    S = sum(Fr(float(v)) ** 2 for v in x)
+    return x, S, T
+
+
+def test_rms_inv_near_a_midpoint(torch, orc):
+    """r at an f32 rounding midpoint.  r on the GPU (compensated f32, about 2^-46
+    relative before its last rounding) and in the oracle (f64) are exact except
+    within that distance of a midpoint: there either may take either neighbour,
+    so only that is asserted (and which one each took is reported).  2^-40 away
+    from the midpoint both must give the correctly rounded value."""
+    from fractions import Fraction as Fr
+
+    from block_quantized_decode_rmsnorm_gb300 import api
+
+    lo, hi = np.float32(1.0), np.nextafter(np.float32(1.0), np.float32(2.0))
+    mid = 1 + Fr(1, 2 ** 24)
+    for offset, must_be_exact in ((0.0, False), (2.0 ** -40, True), (-(2.0 ** -40), True)):
+        x, S, T = _near_midpoint_row(offset)
+        assert 0 <= T - S < T / 2 ** 70  # the construction hit its target
+        # exact r = 1/sqrt(S/1024) lies above the midpoint iff S mid^2 < 1024
+        correct = hi if S * mid * mid < 1024 else lo
+        g = np.ones(1024, np.float32)
+        inv = torch.empty((1,), dtype=torch.float32, device="cuda")
+        api.rmsnorm_quantize(to_dev(x, torch), to_dev(g, torch), 0.0, inv_rms=inv)
+        torch.cuda.synchronize()
+        r_gpu = inv.cpu().numpy()[0]
+        _, _, r_orc, _ = orc.rmsnorm_quantize(x, g, 0.0)
+        assert r_gpu in (lo, hi) and r_orc in (lo, hi), (r_gpu, r_orc)
+        if must_be_exact:
+            assert r_gpu == correct and r_orc == correct, (offset, r_gpu, r_orc, correct)
+        else:
+            print(f"at the midpoint: gpu {r_gpu!r}, oracle {r_orc!r}, correctly rounded {correct!r}")
