@@ -39,7 +39,7 @@ struct Bf16Params {
     int epi;
 };
 
-constexpr int BF16_THREADS = 128;
+constexpr int BF16_THREADS = 512;
 
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
