@@ -396,6 +396,18 @@ def config_summary(torch, pk, probe_gbs: float, variants: bool = False) -> tuple
         r, algo, _ = gemv(262144, 1024, b)
         cfg[f"4_head_262144x1024_b{b}"] = hbm_entry(r, algo)
 
+    # next step 4: the headline step with the activation rotated in the fused
+    # gate|up kernel (qg_decode_ffn_q8_0_rotated), 24 layers, one graph
+    layers, x0 = make_layers(torch, 24)
+    buf = api.FFNBuffers.allocate(HIDDEN, FFN, "cuda")
+    xr = torch.from_numpy(x0).cuda()
+    gr = capture(torch, lambda: [api.qg_decode_ffn_q8_0_rotated(xr, xr, ly, buf, EPS) for ly in layers])
+    t_r = replay_trials(torch, gr, 1)["median"]
+    del gr, layers
+    gbs = 24 * LAYER_BYTES / t_r / 1e9
+    cfg["next4_rotated_decode_step_24_layers"] = {"us": round(t_r * 1e6, 2), "GB/s": round(gbs, 1),
+                                                  "frac_copy_peak": round(gbs / hbm, 4)}
+
     # 3: bf16 gate|up 18432x2560, RMSNorm in front, SiLU*u behind
     bc = synth.bf16_case(0)
     w0 = api.bf16_from_bits(bc["w"])

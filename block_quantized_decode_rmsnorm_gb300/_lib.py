@@ -41,6 +41,7 @@ SIGNATURES = {
     "qg_ffn_up_q8_0": (ST, [P, P, I64, F32, P, P, I64, P, P, P, P, P, P, P]),
     "qg_decode_ffn_q8_0": (ST, [P, P, I64, I64, F32, P, P, P, P, P, P, P, P]),
     "qg_decode_ffn_q8_0_out": (ST, [P, P, P, I64, I64, F32, P, P, P, P, P, P, P, P]),
+    "qg_decode_ffn_q8_0_rotated": (ST, [P, P, P, I64, I64, F32, P, P, P, P, P, P, P, P, P, P]),
     "qg_decode_layer_q8_0": (ST, [P, P, I32, P, P, P, I64, I64, F32, P, P, P, P, P, P, P, P]),
     "qg_decode_layer_partials": (I32, [I64, I64]),
     "qg_decode_layer_finish": (ST, [P, P, I32, I64, P, P]),

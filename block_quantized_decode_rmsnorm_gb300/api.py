@@ -466,9 +466,11 @@ def decode_ffn_q8_0(x: torch.Tensor, layer: FFNLayer, buf: FFNBuffers, eps: floa
 def decode_ffn_q8_0_rotated(x: torch.Tensor, layer: FFNLayer, buf: FFNBuffers, eps: float = 1e-6,
                             stream=None) -> None:
     """decode_ffn_q8_0 with the normalised activation rotated once (order-128
-    Walsh-Hadamard per block) before it is quantized; the stacked gate|up weights
-    of `layer` are the rotated ones (W H^T / 128, quantized at load time), so both
-    halves read the one rotated activation.
+    Walsh-Hadamard per block) before it is quantized, in four launches
+    (rmsnorm_hadamard_quantize, the stacked gate|up GEMV with SiLU*u, Q8_0 of h,
+    down with the residual); the stacked gate|up weights of `layer` are the
+    rotated ones (W H^T / 128, quantized at load time), so both halves read the
+    one rotated activation.
 
     "Filling in the blanks: Inference using Phobos", PrismML Ternary-Bonsai-2-27B:
     the rotated activation is computed once and shared by every projection that
@@ -484,6 +486,24 @@ def decode_ffn_q8_0_rotated(x: torch.Tensor, layer: FFNLayer, buf: FFNBuffers, e
     _lib.call("quantize_act_q8_0", buf.h.data_ptr(), 1, ffn, buf.hq.data_ptr(), buf.hd.data_ptr(), s)
     _lib.call("qgemv_q8_0", layer.down.qs.data_ptr(), layer.down.d.data_ptr(), hidden, ffn, buf.hq.data_ptr(),
               buf.hd.data_ptr(), 1, QG_EPI_RESIDUAL_ADD, x.data_ptr(), x.data_ptr(), s)
+
+
+def qg_decode_ffn_q8_0_rotated(x_in: torch.Tensor, x_out: torch.Tensor, layer: FFNLayer, buf: FFNBuffers,
+                               eps: float = 1e-6, export_codes: bool = False, stream=None) -> None:
+    """The same layer in two launches: the fused gate|up kernel rotates the
+    normalised activation itself (each CTA, one 128-value rotation per warp),
+    quantizes it and shares it between the stacked halves; then the down GEMV
+    with the residual.  With export_codes, buf.xq / buf.xd receive the rotated
+    activation's codes and scales."""
+    hidden = layer.gamma.shape[-1]
+    ffn = layer.down.k
+    _need_reachable(x_in, "x_in", (hidden,))
+    _need_reachable(x_out, "x_out", (hidden,))
+    _lib.call("qg_decode_ffn_q8_0_rotated", x_in.data_ptr(), x_out.data_ptr(), layer.gamma.data_ptr(), hidden, ffn,
+              float(eps), layer.gate_up.qs.data_ptr(), layer.gate_up.d.data_ptr(), layer.down.qs.data_ptr(),
+              layer.down.d.data_ptr(), buf.h.data_ptr(), buf.hq.data_ptr(), buf.hd.data_ptr(),
+              buf.xq.data_ptr() if export_codes else None, buf.xd.data_ptr() if export_codes else None,
+              _stream_handle(stream))
 
 
 def qg_ffn_up_q8_0(x: torch.Tensor, gamma: torch.Tensor, w: Q8Weight, eps: float = 1e-6, h=None, hq=None, hd=None,

@@ -26,6 +26,9 @@ bool ffn_up_supported(int64_t k, int64_t half);
 cudaError_t launch_ffn_up(const float *, const float *, int64_t, float, const int8_t *, const uint16_t *, int64_t,
                           float *, int8_t *, uint16_t *, int8_t *, uint16_t *, float *, cudaStream_t);
 bool prefetch_supported(int64_t n_rows, int64_t k);
+bool ffn_up_rotated_supported(int64_t k, int64_t half);
+cudaError_t launch_ffn_up_rotated(const float *, const float *, int64_t, float, const int8_t *, const uint16_t *,
+                                  int64_t, float *, int8_t *, uint16_t *, int8_t *, uint16_t *, cudaStream_t);
 bool decode_layer_supported(int64_t k, int64_t half);
 int decode_layer_partials(int64_t half);
 constexpr int kMaxLayerPartials = 16;
@@ -328,6 +331,29 @@ qg_status qg_decode_ffn_q8_0_out(const float *x_in, float *x_out, const float *g
                                                   x_out, stream));
     return from_cuda(
         qg::launch_gemv_q8_0(wdn_qs, wdn_d, hidden, ffn, hq, hd, 1, QG_EPI_RESIDUAL_ADD, x_in, x_out, stream));
+}
+
+qg_status qg_decode_ffn_q8_0_rotated(const float *x_in, float *x_out, const float *gamma, int64_t hidden,
+                                     int64_t ffn, float eps, const int8_t *wgu_qs, const uint16_t *wgu_d,
+                                     const int8_t *wdn_qs, const uint16_t *wdn_d, float *h, int8_t *hq, uint16_t *hd,
+                                     int8_t *xq_out, uint16_t *xd_out, qg_stream_t stream)
+{
+    if (hidden <= 0 || hidden % 32 != 0 || ffn <= 0 || ffn % 32 != 0 || ffn > kMaxRows / 2 || ffn > kMaxK)
+        return QG_ERR_SHAPE;
+    if (!(eps >= 0.0f)) return QG_ERR_SHAPE;
+    if (!qg::ffn_up_rotated_supported(hidden, ffn) || !qg::prefetch_supported(hidden, ffn)) return QG_ERR_UNSUPPORTED;
+    if (!x_in || !x_out || !gamma || !wgu_qs || !wgu_d || !wdn_qs || !wdn_d || !h || !hq || !hd) return QG_ERR_NULL;
+    if (!aligned(x_in, 16) || !aligned(x_out, 16) || !aligned(gamma, 16) || !aligned(wgu_qs, 32) ||
+        !aligned(wgu_d, 16) || !aligned(wdn_qs, 32) || !aligned(wdn_d, 16) || !aligned(h, 16) || !aligned(hq, 32) ||
+        !aligned(hd, 2) || !aligned(xq_out, 16) || !aligned(xd_out, 2))
+        return QG_ERR_ALIGN;
+    const size_t xb = static_cast<size_t>(hidden) * sizeof(float);
+    if (x_in != x_out && overlap(x_in, xb, x_out, xb)) return QG_ERR_SHAPE;
+    qg_status st = from_cuda(qg::launch_ffn_up_rotated(x_in, gamma, hidden, eps, wgu_qs, wgu_d, ffn, h, hq, hd, xq_out,
+                                                       xd_out, stream));
+    if (st != QG_OK) return st;
+    return from_cuda(
+        qg::launch_gemv_prefetch(wdn_qs, wdn_d, hidden, ffn, hq, hd, QG_EPI_RESIDUAL_ADD, x_in, x_out, stream));
 }
 
 qg_status qg_decode_ffn_q8_0(float *x, const float *gamma, int64_t hidden, int64_t ffn, float eps,

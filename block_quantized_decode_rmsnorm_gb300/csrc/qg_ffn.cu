@@ -62,6 +62,35 @@ __device__ __forceinline__ float block_term(const u32x8 &w, const u32x8 &x, floa
     return fmaf(small_int_to_float(s), dw * dx, acc);
 }
 
+// Order-128 Walsh-Hadamard transform (Sylvester order, unnormalised) of the 128
+// values a warp holds, lane l holding values 4 l .. 4 l + 3: butterflies of
+// strides 1 and 2 in registers, then strides 4 .. 64 across lanes (a + b in the
+// lane holding a, a - b in the lane holding b), in f32, in that order (the order
+// of rmsnorm_hadamard_quantize, so both give the same bits).
+__device__ __forceinline__ float4 hadamard128_lane4(float4 v, int lane)
+{
+    auto bf = [](float &a, float &b) {
+        const float s = __fadd_rn(a, b), d = __fsub_rn(a, b);
+        a = s;
+        b = d;
+    };
+    bf(v.x, v.y);
+    bf(v.z, v.w);
+    bf(v.x, v.z);
+    bf(v.y, v.w);
+#pragma unroll
+    for (int m = 1; m <= 16; m <<= 1) {
+        const bool hi = (lane & m) != 0;
+        const float p0 = __shfl_xor_sync(0xffffffffu, v.x, m), p1 = __shfl_xor_sync(0xffffffffu, v.y, m);
+        const float p2 = __shfl_xor_sync(0xffffffffu, v.z, m), p3 = __shfl_xor_sync(0xffffffffu, v.w, m);
+        v.x = hi ? __fsub_rn(p0, v.x) : __fadd_rn(v.x, p0);
+        v.y = hi ? __fsub_rn(p1, v.y) : __fadd_rn(v.y, p1);
+        v.z = hi ? __fsub_rn(p2, v.z) : __fadd_rn(v.z, p2);
+        v.w = hi ? __fsub_rn(p3, v.w) : __fadd_rn(v.w, p3);
+    }
+    return v;
+}
+
 __device__ __forceinline__ void zero(u32x8 &w)
 {
 #pragma unroll
@@ -140,9 +169,10 @@ __host__ __device__ constexpr size_t ffn_up_smem_bytes(int k, bool down = false)
 // After the wait there are two CTA barriers: the norm statistic's (which also
 // checks the staged slab) and the row partials'; warp 0 then forms h = SiLU(g) u
 // and its Q8_0 block.
-template <int NBL, bool DOWN>
+template <int NBL, bool DOWN, bool ROT = false>
 __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
 {
+    static_assert(!ROT || (NBL == 1 && !DOWN), "the rotated form serves k <= 1024, two-launch layers");
     constexpr int NW = 8 * NBL;  // warps per CTA
     extern __shared__ __align__(16) uint8_t smem[];
     const int K = p.k, nb = p.nb, KP = K + 16;
@@ -204,7 +234,10 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
     pdl_wait();
 
     const int wl = warp & 7, wh = warp >> 3;
-    const int xb = wl + 8 * (lane >> 3) + 32 * wh;  // block of this thread's four x values (and of its dots)
+    // block of this thread's four x values (and of its dots); the rotated form
+    // gives warp w the blocks 4 w .. 4 w + 3, one 128-value block of the rotation,
+    // lane l holding its values 4 l .. 4 l + 3
+    const int xb = ROT ? 4 * wl + (lane >> 3) : wl + 8 * (lane >> 3) + 32 * wh;
     const int xo = 32 * xb + 4 * (lane & 7);        // their offset in x
     const bool live = xb < nb;
     const int rg = lane & 7;                        // this lane's rows: rg + 8 i
@@ -284,6 +317,7 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
             v.z = __fmul_rn(__fmul_rn(xv4.z, r), g4.z);
             v.w = __fmul_rn(__fmul_rn(xv4.w, r), g4.w);
         }
+        if constexpr (ROT) v = hadamard128_lane4(v, lane);
         float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
@@ -548,10 +582,10 @@ bool decode_layer_supported(int64_t k, int64_t half)
            half / 32 / layer_cluster(half) <= kMaxLayerPartials;
 }
 
-template <int NBL, bool DOWN>
+template <int NBL, bool DOWN, bool ROT = false>
 static cudaError_t ffn_up_attr()
 {
-    return opt_in_smem(reinterpret_cast<const void *>(ffn_up_kernel<NBL, DOWN>), static_cast<int>(kMaxSmem));
+    return opt_in_smem(reinterpret_cast<const void *>(ffn_up_kernel<NBL, DOWN, ROT>), static_cast<int>(kMaxSmem));
 }
 
 static FfnUpParams ffn_up_params(const float *x, const float *gamma, int64_t k, float eps, const int8_t *w_qs,
@@ -602,6 +636,26 @@ cudaError_t launch_ffn_up(const float *x, const float *gamma, int64_t k, float e
     p.xd_out = xd_out;
     p.r_out = r_out;
     return launch_ffn_up_impl<false>(p, s);
+}
+
+// The rotated form: hidden a multiple of 128 up to 1024 (one rotation block per
+// warp), otherwise as ffn_up_supported.
+bool ffn_up_rotated_supported(int64_t k, int64_t half)
+{
+    return k % 256 == 0 && k <= 1024 && ffn_up_supported(k, half);
+}
+
+cudaError_t launch_ffn_up_rotated(const float *x, const float *gamma, int64_t k, float eps, const int8_t *w_qs,
+                                  const uint16_t *w_d, int64_t half, float *h, int8_t *hq, uint16_t *hd,
+                                  int8_t *xq_out, uint16_t *xd_out, cudaStream_t s)
+{
+    if (half == 0) return cudaSuccess;
+    FfnUpParams p = ffn_up_params(x, gamma, k, eps, w_qs, w_d, half, h, hq, hd);
+    p.xq_out = xq_out;
+    p.xd_out = xd_out;
+    if (cudaError_t e = ffn_up_attr<1, false, true>(); e != cudaSuccess) return e;
+    return launch_pdl(ffn_up_kernel<1, false, true>, dim3(static_cast<unsigned>(half / 32)), dim3(256),
+                      ffn_up_smem_bytes(p.k, false), s, p);
 }
 
 int decode_layer_partials(int64_t half) { return static_cast<int>(half / 32 / layer_cluster(half)); }

@@ -287,6 +287,31 @@ QG_API qg_status qg_decode_ffn_q8_0_out(const float *x_in, float *x_out, const f
                                         uint16_t *hd, qg_stream_t stream);
 
 /*
+ * qg_decode_ffn_q8_0_rotated - qg_decode_ffn_q8_0_out with the normalised
+ * activation rotated before it is quantized ([Phobos] PrismML
+ * Ternary-Bonsai-2-27B: the rotated activation is computed once and shared by
+ * every projection that reads the input; here by both halves of the stacked
+ * gate|up), in two launches:
+ *   z = H x_hat per block of 128 (as rmsnorm_hadamard_quantize: x_hat =
+ *       (x r) gamma, the order-128 Walsh-Hadamard matrix, unnormalised),
+ *   (g|u) = gate|up(Q8_0(z)), h = SiLU(g) u, x_out = x_in + down(Q8_0(h)).
+ * The stacked gate|up weights are the rotated ones (W H^T / 128, quantized at
+ * load time), so that W x_hat = (W H^T / 128) z.
+ *   xq_out, xd_out: optional (NULL): the rotated activation's codes int8[hidden]
+ *          (16-byte aligned) and scales binary16[hidden/32].
+ *   hidden a multiple of 256 up to 1024 (one rotation block per warp); ffn as
+ *   qg_decode_ffn_q8_0 with the down weights served by the staged GEMV (ffn a
+ *   multiple of 256 up to 4096); other arguments and errors as
+ *   qg_decode_ffn_q8_0_out.
+ */
+QG_API qg_status qg_decode_ffn_q8_0_rotated(const float *x_in, float *x_out, const float *gamma,
+                                            int64_t hidden, int64_t ffn, float eps,
+                                            const int8_t *wgu_qs, const uint16_t *wgu_d,
+                                            const int8_t *wdn_qs, const uint16_t *wdn_d, float *h,
+                                            int8_t *hq, uint16_t *hd, int8_t *xq_out, uint16_t *xd_out,
+                                            qg_stream_t stream);
+
+/*
  * qg_decode_layer_q8_0 - one decode feed-forward block in ONE launch, its
  * input and output each held unreduced as a base vector plus partial vectors:
  *   x      = r_in + p_in[0] + ... + p_in[n_in - 1]        (f32, in that order)

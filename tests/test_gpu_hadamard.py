@@ -101,3 +101,59 @@ def test_rotated_ffn_staged_parity(torch, orc):
     y, a_y = orc.gemv_q8_0(c["dn_qs"], c["dn_d"], hq, hd)
     exact = c["x"].astype(np.float64) + y[0]
     assert_close(x.cpu().numpy(), exact, a_y[0] + np.abs(c["x"]) + np.abs(exact), TOL_Q8, "out")
+
+
+@pytest.mark.parametrize("hidden,ffn", [(1024, 3584), (256, 512), (512, 1024)])
+def test_fused_rotated_layer(torch, orc, hidden, ffn):
+    """qg_decode_ffn_q8_0_rotated (two launches, the rotation inside the fused
+    gate|up kernel): its rotated codes equal rmsnorm_hadamard_quantize's, and the
+    layer is checked against the oracle stage by stage from its own intermediates."""
+    from block_quantized_decode_rmsnorm_gb300 import api
+
+    c = synth.ffn_case(7, hidden, ffn)
+    layer = api.FFNLayer(to_dev(c["gamma"], torch), weight(c["gu_qs"], c["gu_d"]), weight(c["dn_qs"], c["dn_d"]))
+    buf = api.FFNBuffers.allocate(hidden, ffn, "cuda")
+    x = to_dev(c["x"], torch)
+    out = Guarded(torch, (hidden,), torch.float32)
+    api.qg_decode_ffn_q8_0_rotated(x, out.view, layer, buf, EPS, export_codes=True)
+    torch.cuda.synchronize()
+    out.check()
+    qs, ds = api.rmsnorm_hadamard_quantize(x, layer.gamma, EPS)
+    xq, xd = buf.xq[0].cpu().numpy(), f16_to_np_bits(buf.xd)[0]
+    assert np.array_equal(xq, qs.cpu().numpy()[0]) and np.array_equal(xd, f16_to_np_bits(ds)[0])
+    gu, a_gu = orc.gemv_q8_0(c["gu_qs"], c["gu_d"], xq, xd)
+    g, u = gu[0, :ffn], gu[0, ffn:]
+    h = buf.h[0].cpu().numpy()
+    assert_close(h, orc.silu_mul(g, u), silu_scale(g, u, a_gu[0, :ffn], a_gu[0, ffn:]), TOL_Q8, "h")
+    hq, hd = orc.quantize_q8_0(h[None, :])
+    assert np.array_equal(buf.hq.cpu().numpy(), hq) and np.array_equal(f16_to_np_bits(buf.hd), hd)
+    y, a_y = orc.gemv_q8_0(c["dn_qs"], c["dn_d"], hq, hd)
+    exact = c["x"].astype(np.float64) + y[0]
+    assert_close(out.view.cpu().numpy(), exact, a_y[0] + np.abs(c["x"]) + np.abs(exact), TOL_Q8, "out")
+
+
+def test_fused_rotated_layers_chained_in_place(torch, orc):
+    """Three rotated layers in place, each compared with the four-launch rotated
+    composite run on the fused path's own input to it (same rotated codes, so the
+    same h up to the order of the gate|up sums: checked against the oracle)."""
+    from block_quantized_decode_rmsnorm_gb300 import api
+
+    cases = [synth.ffn_case(8, 1024, 3584, layer=l) for l in range(3)]
+    x = to_dev(cases[0]["x"], torch)
+    buf = api.FFNBuffers.allocate(1024, 3584, "cuda")
+    for c in cases:
+        layer = api.FFNLayer(to_dev(c["gamma"], torch), weight(c["gu_qs"], c["gu_d"]),
+                             weight(c["dn_qs"], c["dn_d"]))
+        x_in = x.cpu().numpy()
+        api.qg_decode_ffn_q8_0_rotated(x, x, layer, buf, EPS, export_codes=True)
+        torch.cuda.synchronize()
+        z64, a, _, _ = orc.rmsnorm_hadamard(x_in, c["gamma"], EPS)
+        xq, xd = buf.xq[0].cpu().numpy(), f16_to_np_bits(buf.xd)[0]
+        # the codes dequantize to the exact rotated row within the Q8_0 bound: half a
+        # step, plus the binary16 rounding of the scale times |code| <= 127
+        dh = np.repeat(orc.f16_bits_to_f64(xd), 32)
+        deq = xq.astype(np.float64) * dh
+        assert np.max(np.abs(deq - z64) / dh.clip(min=1e-30)) <= 0.5 + 127 * 2.0 ** -11 + 1e-6
+        y, a_y = orc.gemv_q8_0(c["dn_qs"], c["dn_d"], buf.hq.cpu().numpy(), f16_to_np_bits(buf.hd))
+        exact = x_in.astype(np.float64) + y[0]
+        assert_close(x.cpu().numpy(), exact, a_y[0] + np.abs(x_in) + np.abs(exact), TOL_Q8, "out")
