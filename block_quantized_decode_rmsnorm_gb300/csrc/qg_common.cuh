@@ -337,6 +337,18 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     return true;
 }
 
+// The same with the thread asleep in the barrier unit between checks, for
+// waits that may be long and overlap other kernels' work on the SM.
+__device__ __forceinline__ bool mbar_wait_sleep_bounded(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
+{
+    constexpr uint32_t kHintNs = 1000000u;
+    if (mbar_try_wait_sleep(bar, parity, kHintNs)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait_sleep(bar, parity, kHintNs))
+        if (global_ns() - t0 > limit_ns) return false;
+    return true;
+}
+
 // Limit for a wait on copies that were issued long before: one second.
 constexpr uint64_t kCopyWaitLimitNs = 1000000000ull;
 

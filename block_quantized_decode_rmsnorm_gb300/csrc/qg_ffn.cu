@@ -13,12 +13,21 @@
 // needs a full reduction of its predecessor's output.  Launched as separate
 // grids, every step pays launch ramp-up plus one DRAM round trip before its
 // weights arrive.  Here each kernel is a single wave whose CTAs copy their whole
-// weight slab (values, scales, gain) into shared memory with cp.async issued
-// BEFORE griddepcontrol.wait (~30-75 KB per CTA), and trigger their dependent
-// launch on entry.  Kernels further down the stream therefore become resident
-// and stream their weights while their predecessors still compute; after the
-// wait only on-chip work remains.  (Plain loads into registers would not do:
-// the compiler may legally sink read-only loads below the wait.)
+// weight slab (values, scales, gain) into shared memory with bulk copies issued
+// BEFORE griddepcontrol.wait (~30-85 KB per CTA).  Kernels further down the
+// stream therefore become resident and stream their weights while their
+// predecessors still compute; after the wait only on-chip work remains.
+// (Plain loads into registers would not do: the compiler may legally sink
+// read-only loads below the wait.)
+//
+// When each kernel releases its dependent launch is tuned for the decode layer
+// (gate|up, then down, then the next layer's gate|up): the GEMV releases it on
+// entry, so the next layer's gate|up stages its slab during this layer's whole
+// chain, but the gate|up kernel releases the down GEMV only once its own wait
+// has returned, so that the GEMV's CTAs are not resident on the SMs before the
+// gate|up chain starts.  Measured over 24 layers on GB300: 102.5 us a step,
+// against 117 with both releases on entry, 137 with both after the wait and 147
+// with the gate|up release on entry and the GEMV's after its wait.
 //
 // Shared-memory reads are laid out so that every quarter-warp phase touches 32
 // distinct banks: in the GEMV kernels lane j reads the 32-byte block j of a row
@@ -146,11 +155,13 @@ __host__ __device__ constexpr size_t ffn_up_smem_bytes(int k, bool down = false)
 {
     // values [64][k + 16] | scales [64][k/32] u16 | gamma [k] f32 | row partials [warps][64] f32
     // | warp partial pairs [2 * 16] f32
-    // | (one-launch layer) down column block [k][32] int8 | its scales [k] u16 | this CTA's
-    //   terms of every output [k] f32 | h codes [32] | h scale f32 (16 B)
+    // | (two-launch) the scales again, f32, in dot order [k/32][64]
+    // | (one-launch layer) down column block [k][32] int8 | its scales [k] u16 | h codes [32]
+    //   | h scale f32 (16 B); this CTA's terms of every output, [k] f32, reuse the values' space
+    //   (dead once h is formed), so that two CTAs fit on an SM for k = 1024
     return static_cast<size_t>(64) * (k + 16) + 64 * (k / 32) * 2 + 4 * k +
            static_cast<size_t>(2048) * ((k + 1023) / 1024) + 4 * 32 +
-           (down ? static_cast<size_t>(32) * k + 2 * k + 4 * k + 32 + 16 : 0);
+           (down ? static_cast<size_t>(32) * k + 2 * k + 32 + 16 : static_cast<size_t>(8) * k);
 }
 
 // One CTA per 32-output block of h (rows o..o+31 of gate and of up).
@@ -181,11 +192,13 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
     float *s_gamma = reinterpret_cast<float *>(smem + 64 * KP + 128 * nb);
     float *s_red = s_gamma + K;       // [NW][64]
     float *s_part = s_red + NW * 64;  // [2 * NW]
-    int8_t *s_dn = reinterpret_cast<int8_t *>(s_part + 32);        // [K][32] (DOWN)
+    // (!DOWN) [nb][2][8][4]: scale of row g + 8 i, block b at ((2 b + i / 4) 8 + g) 4 + i % 4
+    float *s_wdf = s_part + 32;
+    int8_t *s_dn = reinterpret_cast<int8_t *>(s_part + 32);         // [K][32] (DOWN)
     uint16_t *s_dnd = reinterpret_cast<uint16_t *>(s_dn + 32 * K);  // [K]     (DOWN)
-    float *s_out = reinterpret_cast<float *>(s_dnd + K);            // [K]     (DOWN)
-    int8_t *s_hq = reinterpret_cast<int8_t *>(s_out + K);           // [32]    (DOWN)
+    int8_t *s_hq = reinterpret_cast<int8_t *>(s_dnd + K);           // [32]    (DOWN)
     float *s_hd = reinterpret_cast<float *>(s_hq + 32);             // [1]     (DOWN)
+    float *s_out = reinterpret_cast<float *>(smem);                 // [K]     (DOWN, over the values)
 
     const int t = threadIdx.x;
     const int lane = t & 31;
@@ -193,7 +206,6 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
     const int64_t ob = static_cast<int64_t>(blockIdx.x) * 32;
 
     __shared__ __align__(8) uint64_t s_bar;
-    pdl_trigger();
 
     // ---- stage everything that does not depend on the previous kernel -------
     // Bulk copies issued by one thread are serviced one after another, so they
@@ -231,7 +243,27 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
         }
     }
 
+    // Still before the wait (the CTA has nothing else to do): once the slab has
+    // landed, the gate|up scales go to f32 in the order the dots read them, so a
+    // lane's eight scales are two 16-byte words and a quarter-warp reads 128
+    // contiguous bytes.  The threads sleep in the barrier unit until then: a spin
+    // here would take issue slots from the kernel whose chain runs on this SM
+    // (measured: 2 us a step).  A copy that has not landed within the limit
+    // leaves NaN outputs for this block.
+    const bool ok = mbar_wait_sleep_bounded(&s_bar, 0, kCopyWaitLimitNs);
+    if (!DOWN && ok) {
+        for (int e = t; e < 8 * nb; e += blockDim.x) {
+            const int b = e >> 3, g = e & 7;
+            float f[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) f[i] = h2f(s_wd[(g + 8 * i) * nb + b]);
+            *reinterpret_cast<float4 *>(s_wdf + (2 * b * 8 + g) * 4) = make_float4(f[0], f[1], f[2], f[3]);
+            *reinterpret_cast<float4 *>(s_wdf + ((2 * b + 1) * 8 + g) * 4) = make_float4(f[4], f[5], f[6], f[7]);
+        }
+    }
+    const bool staged = __syncthreads_and(ok);
     pdl_wait();
+    pdl_trigger();  // the dependent (the layer's down GEMV) only now: see the top of the file
 
     const int wl = warp & 7, wh = warp >> 3;
     // block of this thread's four x values (and of its dots); the rotated form
@@ -277,10 +309,7 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
         s_part[2 * warp] = acc.hi;
         s_part[2 * warp + 1] = acc.lo;
     }
-    // The same barrier publishes the staged slab (thread 0 has seen it land,
-    // normally long ago).  A copy that has not landed within the limit leaves
-    // NaN outputs for this block.
-    const bool staged = __syncthreads_and(t != 0 || mbar_wait_bounded(&s_bar, 0, kCopyWaitLimitNs));
+    __syncthreads();
     if (!staged) {
         if (warp == 0) {
             p.h[ob + lane] = __int_as_float(0x7fc00000);
@@ -342,12 +371,27 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
 #pragma unroll
     for (int s = 0; s < 8; ++s) xw.v[s] = __shfl_sync(0xffffffffu, xc, src + s);
     const float xs = __shfl_sync(0xffffffffu, xdf, src);
+    // all sixteen 16-byte reads of the eight rows are issued before the first dot
     float part[8];
+    if (DOWN && live) {
+        // (the one-launch layer keeps no f32 copy of the scales: shared memory)
+        u32x8 wv[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int row = rg + 8 * i;
-        part[i] = live ? block_term(ld_block_halves(s_w + row * KP + xb * QK, 0), xw, h2f(s_wd[row * nb + xb]), xs, 0.0f)
-                       : 0.0f;
+        for (int i = 0; i < 8; ++i) wv[i] = ld_block_halves(s_w + (rg + 8 * i) * KP + xb * QK, 0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) part[i] = block_term(wv[i], xw, h2f(s_wd[(rg + 8 * i) * nb + xb]), xs, 0.0f);
+    } else if (live) {
+        const float4 sa = *reinterpret_cast<const float4 *>(s_wdf + ((2 * xb) * 8 + rg) * 4);
+        const float4 sb = *reinterpret_cast<const float4 *>(s_wdf + ((2 * xb + 1) * 8 + rg) * 4);
+        const float sc[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+        u32x8 wv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) wv[i] = ld_block_halves(s_w + (rg + 8 * i) * KP + xb * QK, 0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) part[i] = block_term(wv[i], xw, sc[i], xs, 0.0f);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) part[i] = 0.0f;
     }
     // the four lane groups of a row: offset 16 (block bit 4), then 8 (bit 3); a
     // lane keeps half of its values each time and ends with rows rg + 8 (2 (lane / 8) + k)
@@ -496,20 +540,18 @@ __global__ void __launch_bounds__(256) gemv_prefetch_kernel(const PrefetchParams
     pdl_wait();
 
     // The activation and, for the residual epilogue, this lane's residual
-    // value are loaded together, so both L2 round trips overlap.
+    // value are all requested before any of them is used, so their L2 round
+    // trips overlap: the loads are unconditional (a block past the row's end
+    // reads the last block again) and nothing converts a loaded value until the
+    // last request is out.  Blocks past the end are zeroed afterwards.
     const int c0 = lane_half(lane);
     u32x8 xv[NBL];
-    float xs[NBL];
+    uint16_t xdr[NBL];
 #pragma unroll
     for (int j = 0; j < NBL; ++j) {
-        const int blk = lane + 32 * j;
-        if (blk < nb) {
-            xv[j] = ld_block_halves(p.xq + blk * QK, c0);
-            xs[j] = h2f(p.xd[blk]);
-        } else {
-            zero(xv[j]);
-            xs[j] = 0.0f;
-        }
+        const int blk = min(lane + 32 * j, nb - 1);
+        xv[j] = ld_block_halves(p.xq + blk * QK, c0);
+        xdr[j] = p.xd[blk];
     }
     // lane l of warp w holds the residual of row w + l * nw (rows of this CTA)
     float res = 0.0f;
@@ -524,24 +566,28 @@ __global__ void __launch_bounds__(256) gemv_prefetch_kernel(const PrefetchParams
         mbar_wait_bounded(&s_bar, 0, kCopyWaitLimitNs);
         return;
     }
+    float xs[NBL];
+#pragma unroll
+    for (int j = 0; j < NBL; ++j) {
+        const bool in = lane + 32 * j < nb;
+        xs[j] = in ? h2f(xdr[j]) : 0.0f;
+        if (!in) zero(xv[j]);
+    }
 
     for (int rr = warp, it = 0; rr < nrow; rr += nw, ++it) {
+        // a block past the end: zero codes and zero scales, so its term adds +0
         u32x8 wr[NBL];
-        float wsc[NBL];
+        uint16_t wsr[NBL];
 #pragma unroll
         for (int j = 0; j < NBL; ++j) {
-            const int blk = lane + 32 * j;
-            if (blk < nb) {
-                wr[j] = ld_block_halves(s_w + rr * K + blk * QK, c0);
-                wsc[j] = h2f(s_wd[rr * nb + blk]);
-            } else {
-                zero(wr[j]);
-                wsc[j] = 0.0f;
-            }
+            const int blk = min(lane + 32 * j, nb - 1);
+            wr[j] = ld_block_halves(s_w + rr * K + blk * QK, c0);
+            wsr[j] = s_wd[rr * nb + blk];
         }
         float acc = 0.0f;
 #pragma unroll
-        for (int j = 0; j < NBL; ++j) acc = block_term(wr[j], xv[j], wsc[j], xs[j], acc);
+        for (int j = 0; j < NBL; ++j)
+            acc = block_term(wr[j], xv[j], lane + 32 * j < nb ? h2f(wsr[j]) : 0.0f, xs[j], acc);
         acc = warp_sum(acc);
         const float rv = __shfl_sync(0xffffffffu, res, it & 31);
         if (lane == 0) {

@@ -340,7 +340,7 @@ QG_API qg_status qg_decode_ffn_q8_0_rotated(const float *x_in, float *x_out, con
  *          qg_q8_0_column_blocks: values int8[ffn/32][hidden][32] (32-byte
  *          aligned), scales binary16[ffn/32][hidden] (16-byte aligned).
  *   hidden a multiple of 256 whose one-launch working set fits one CTA's shared
- *   memory (hidden <= 1792 on GB300); ffn a multiple of 32 with P <= 16
+ *   memory (hidden <= 2048 on GB300); ffn a multiple of 32 with P <= 16
  *   (QG_ERR_UNSUPPORTED otherwise).  A CTA whose staged copies stall beyond
  *   one second contributes NaN instead of hanging.
  * A stack of layers ping-pongs two (r, p) pairs, layer 0 with n_in = 0, and

@@ -257,9 +257,10 @@ def test_one_launch_layer_argument_errors(lib):
                                                              FAKE, FAKE, FAKE, FAKE, FAKE, None)
     assert lib.qg_decode_layer_partials(1024, 3584) == 14
     assert lib.qg_decode_layer_partials(256, 96) == 3
-    assert lib.qg_decode_layer_partials(2048, 1024) == -1
-    # working set beyond a CTA's shared memory, hidden not a multiple of 256, too many partials
-    assert f(*args(RI, PI, 14, RO, PO, 2048, 1024)) == 4
+    assert lib.qg_decode_layer_partials(2048, 1024) == 4
+    assert lib.qg_decode_layer_partials(2304, 1024) == -1
+    # hidden beyond 2048, hidden not a multiple of 256, too many partials
+    assert f(*args(RI, PI, 14, RO, PO, 2304, 1024)) == 4
     assert f(*args(RI, PI, 14, RO, PO, 992, 3584)) == 4
     assert f(*args(RI, PI, 14, RO, PO, 1024, 32 * 8 * 17)) == 4
     assert f(*args(RI, PI, 17, RO, PO)) == 3
@@ -290,7 +291,7 @@ def test_noalloc_stack_argument_errors(lib):
     assert lib.qg_decode_layer_partials(1024, 4096) == 16
     assert lib.qg_decode_layer_partials(1024, 4096 + 256) == -1
     # unsupported layer shape, negative count
-    assert f(FAKE, FAKE, 1, arr, arr, arr, arr, arr, 2048, 1024, eps, None) == 4
+    assert f(FAKE, FAKE, 1, arr, arr, arr, arr, arr, 2304, 1024, eps, None) == 4
     assert f(FAKE, FAKE, -1, arr, arr, arr, arr, arr, 1024, 3584, eps, None) == 3
     # null pointer arrays / entries, misaligned input
     assert f(FAKE, FAKE, 1, None, arr, arr, arr, arr, 1024, 3584, eps, None) == 1

@@ -54,7 +54,7 @@ def test_column_blocks_bit_exact(torch, orc):
 
 
 # grids of 112, 3, 16, 16 and 6 CTAs: clusters of 8, 1, 8, 8 and 2 (14, 3, 2, 2, 3 partials)
-@pytest.mark.parametrize("hidden,ffn", [(1024, 3584), (256, 96), (1792, 512), (1280, 512), (768, 192)])
+@pytest.mark.parametrize("hidden,ffn", [(1024, 3584), (256, 96), (1792, 512), (2048, 1024), (1280, 512), (768, 192)])
 def test_one_launch_layer(torch, orc, hidden, ffn):
     from block_quantized_decode_rmsnorm_gb300 import api
 
