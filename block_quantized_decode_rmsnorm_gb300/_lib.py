@@ -45,6 +45,7 @@ SIGNATURES = {
     "qg_decode_layer_q8_0": (ST, [P, P, I32, P, P, P, I64, I64, F32, P, P, P, P, P, P, P, P]),
     "qg_decode_layer_partials": (I32, [I64, I64]),
     "qg_decode_layer_finish": (ST, [P, P, I32, I64, P, P]),
+    "qg_copy_stalls": (ST, [ctypes.POINTER(ctypes.c_uint32), I32]),
     "qg_decode_layers_q8_0_noalloc": (ST, [P, P, I32, P, P, P, P, P, I64, I64, F32, P]),
     "qg_decode_stack_workspace_bytes": (I64, [I64, I64]),
     "qg_decode_stack_max_layers": (I32, []),

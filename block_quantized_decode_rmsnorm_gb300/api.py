@@ -685,6 +685,16 @@ def qg_decode_layers_q8_0_noalloc(x_in: torch.Tensor, layers, eps: float = 1e-6,
     return x_out
 
 
+def copy_stalls(clear: bool = False) -> int:
+    """Waits of the decode kernels on their staged weight copies that gave up
+    on the current device since the last clear (qg_copy_stalls); 0 normally."""
+    import ctypes
+
+    n = ctypes.c_uint32(0)
+    _lib.call("qg_copy_stalls", ctypes.byref(n), 1 if clear else 0)
+    return int(n.value)
+
+
 def qg_decode_stack_workspace_bytes(hidden: int, ffn: int) -> int:
     n = _lib.load().qg_decode_stack_workspace_bytes(hidden, ffn)
     if n < 0:

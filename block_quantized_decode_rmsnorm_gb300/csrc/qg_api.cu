@@ -58,6 +58,7 @@ cudaError_t launch_prefill_tc(const int8_t *, const uint16_t *, int64_t, int64_t
                               cudaStream_t);
 cudaError_t launch_gemv_prefetch(const int8_t *, const uint16_t *, int64_t, int64_t, const int8_t *, const uint16_t *,
                                  int, const float *, float *, cudaStream_t);
+cudaError_t copy_stalls(uint32_t *count, bool clear);
 struct StackShape {
     int rows_b, grid;
     size_t smem;
@@ -408,6 +409,12 @@ qg_status qg_decode_layer_finish(const float *r, const float *p, int32_t n, int6
     if (!r || (n > 0 && !p) || !x) return QG_ERR_NULL;
     if (!aligned(r, 4) || !aligned(p, 4) || !aligned(x, 4)) return QG_ERR_ALIGN;
     return from_cuda(qg::launch_layer_finish(r, p, n, hidden, x, stream));
+}
+
+qg_status qg_copy_stalls(uint32_t *count, int32_t clear)
+{
+    if (!count) return QG_ERR_NULL;
+    return from_cuda(qg::copy_stalls(count, clear != 0));
 }
 
 qg_status qg_decode_layers_q8_0_noalloc(const float *x_in, float *x_out, int32_t n_layers, const float *const *gamma,

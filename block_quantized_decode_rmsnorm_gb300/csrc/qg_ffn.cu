@@ -62,6 +62,16 @@ namespace qg {
 // shared pieces
 // ---------------------------------------------------------------------------
 
+// Waits on staged weight copies that gave up (the one-second limit) in the
+// kernels of this file, on this GPU: a CTA (gate|up, one-launch layer) or a warp
+// (down GEMV) counts one.  Read and cleared through copy_stalls.
+static __device__ unsigned int g_copy_stalls;
+
+__device__ __forceinline__ void count_copy_stall(bool counter_thread)
+{
+    if (counter_thread) atomicAdd(&g_copy_stalls, 1u);
+}
+
 // S * (d_w * d_x) accumulated the same way as the streaming GEMV kernels.
 __device__ __forceinline__ float block_term(const u32x8 &w, const u32x8 &x, float dw, float dx, float acc)
 {
@@ -311,6 +321,7 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
     }
     __syncthreads();
     if (!staged) {
+        count_copy_stall(t == 0);
         if (warp == 0) {
             p.h[ob + lane] = __int_as_float(0x7fc00000);
             p.hq[ob + lane] = 0;
@@ -561,6 +572,7 @@ __global__ void __launch_bounds__(256) gemv_prefetch_kernel(const PrefetchParams
     // rows (and their residuals), so no CTA barrier is needed.  A copy that has
     // not landed within the limit leaves NaN outputs for this warp's rows.
     if (!mbar_wait_bounded(&s_bar, 0, kCopyWaitLimitNs)) {
+        count_copy_stall(lane == 0);
         for (int rr = warp; rr < nrow; rr += nw)
             if (lane == 0) p.y[r0 + rr] = __int_as_float(0x7fc00000);
         mbar_wait_bounded(&s_bar, 0, kCopyWaitLimitNs);
@@ -705,6 +717,16 @@ cudaError_t launch_ffn_up_rotated(const float *x, const float *gamma, int64_t k,
 }
 
 int decode_layer_partials(int64_t half) { return static_cast<int>(half / 32 / layer_cluster(half)); }
+
+cudaError_t copy_stalls(uint32_t *count, bool clear)
+{
+    unsigned int v = 0;
+    if (cudaError_t e = cudaMemcpyFromSymbol(&v, g_copy_stalls, sizeof(v)); e != cudaSuccess) return e;
+    *count = v;
+    if (!clear || v == 0) return cudaSuccess;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_copy_stalls, &zero, sizeof(zero));
+}
 
 cudaError_t launch_decode_layer(const float *r_in, const float *p_in, int n_in, float *r_out, float *p_out,
                                 const float *gamma, int64_t k, float eps, const int8_t *wgu_qs, const uint16_t *wgu_d,

@@ -218,6 +218,7 @@ QG_API qg_status qgemv_q8_0(const int8_t *w_qs, const uint16_t *w_d, int64_t n_r
  *   w: device bf16 bits [n_rows][k] (read), k a multiple of 8, k <= 16384
  *   x, gamma: device bf16 bits [k] (read)
  *   y: device f32[n_out] (written)
+ *   Each output is summed in one fixed order whatever the shape.
  */
 QG_API qg_status qgemv_bf16(const uint16_t *w, int64_t n_rows, int64_t k, const uint16_t *x,
                      const uint16_t *gamma, float eps, int epilogue,
@@ -342,7 +343,9 @@ QG_API qg_status qg_decode_ffn_q8_0_rotated(const float *x_in, float *x_out, con
  *   hidden a multiple of 256 whose one-launch working set fits one CTA's shared
  *   memory (hidden <= 2048 on GB300); ffn a multiple of 32 with P <= 16
  *   (QG_ERR_UNSUPPORTED otherwise).  A CTA whose staged copies stall beyond
- *   one second contributes NaN instead of hanging.
+ *   one second stops waiting instead of hanging: the outputs are then undefined
+ *   (NaN where it can still write them) and the stall is counted
+ *   (qg_copy_stalls).
  * A stack of layers ping-pongs two (r, p) pairs, layer 0 with n_in = 0, and
  * ends with qg_decode_layer_finish.
  */
@@ -365,6 +368,21 @@ QG_API int32_t qg_decode_layer_partials(int64_t hidden, int64_t ffn);
  */
 QG_API qg_status qg_decode_layer_finish(const float *r, const float *p, int32_t n, int64_t hidden,
                                         float *x, qg_stream_t stream);
+
+/*
+ * qg_copy_stalls - how many waits of the decode kernels on their staged weight
+ * copies gave up (after one second) on the current device since the last clear:
+ * a CTA of the gate|up kernel (qg_ffn_up_q8_0, the qg_decode_ffn_q8_0 family,
+ * qg_decode_layer_q8_0, the layers of qg_decode_layers_q8_0_noalloc) or a warp of
+ * the staging GEMV (their down projection, and qgemv_q8_0 at batch 1 where the
+ * weights fit one wave) counts one.  The outputs of a call with such a stall are
+ * undefined (NaN where the kernel could still write them); 0 in normal
+ * operation.  Not a hang detector for the persistent stack, which reports
+ * through its workspace status word.
+ *   count: host uint32_t (written).  clear != 0 resets the counter after reading.
+ * Reads device memory with a synchronous copy: it waits for the device's work.
+ */
+QG_API qg_status qg_copy_stalls(uint32_t *count, int32_t clear);
 
 /*
  * qg_decode_layers_q8_0_noalloc - a stack of n_layers one-launch decode layers

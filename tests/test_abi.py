@@ -272,6 +272,7 @@ def test_one_launch_layer_argument_errors(lib):
     assert f(*args(RI + 4, PI, 14, RO, PO)) == 2
     assert f(*args(RI, None, 14, RO, PO)) == 1
     assert f(*args(RI, PI, 14, None, PO)) == 1
+    assert lib.qg_copy_stalls(None, 0) == 1
     fin = lib.qg_decode_layer_finish
     assert fin(FAKE, FAKE, 17, 1024, FAKE, None) == 3
     assert fin(FAKE, None, 2, 1024, FAKE, None) == 1

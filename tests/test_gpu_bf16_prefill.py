@@ -31,6 +31,9 @@ def _bf16(bits, torch):
     (100, 4104, True, "none"),         # k not a multiple of 256 or 16: ragged last group
     (64, 8192, True, "residual"),      # several register super-chunks
     (2, 8, False, "silu_mul"),
+    (4865, 1032, False, "none"),       # two rows per task with an odd row count, ragged groups
+    (6000, 2816, True, "residual"),
+    (5000, 256, True, "silu_mul"),
 ])
 def test_bf16_gemv(torch, orc, n, k, norm, epi):
     from block_quantized_decode_rmsnorm_gb300 import api
@@ -56,6 +59,25 @@ def test_bf16_gemv(torch, orc, n, k, norm, epi):
         assert_close(y, exact, a64 + np.abs(res) + np.abs(exact), TOL_BF16, "bf16 residual")
     else:
         assert_close(y, y64, a64, TOL_BF16, "bf16")
+
+
+def test_bf16_outputs_independent_of_matrix_size(torch):
+    """Output o of the 18432 x 2560 gate|up projection depends on gate row o and
+    up row o + 9216 only and is summed in one fixed order, so a 2000-row matrix of
+    the first 1000 gate and up rows (another launch shape) gives the same first
+    1000 outputs bit for bit."""
+    from block_quantized_decode_rmsnorm_gb300 import api
+
+    n, k, F, f = 18432, 2560, 9216, 1000
+    case = synth.bf16_case(n + k, n_rows=n, k=k)
+    w = _bf16(case["w"], torch)
+    x = _bf16(case["x"], torch)
+    g = _bf16(case["gamma"], torch)
+    big = api.qgemv_bf16(w, x, g, EPS, epilogue="silu_mul")
+    small_w = torch.cat([w[:f], w[F:F + f]]).contiguous()
+    small = api.qgemv_bf16(small_w, x, g, EPS, epilogue="silu_mul")
+    torch.cuda.synchronize()
+    assert np.array_equal(big[:f].cpu().numpy().view(np.uint32), small.cpu().numpy().view(np.uint32))
 
 
 def test_bf16_gemv_weights_16_byte_aligned(torch, orc):

@@ -209,6 +209,24 @@ def test_fused_graph_replay(torch, orc):
     assert not np.array_equal(want, eager)
 
 
+def test_no_copy_stalls_in_normal_operation(torch, orc):
+    """The stall counter of the decode kernels reads 0 after eager and replayed
+    layers (every staged copy lands), and clearing it leaves 0."""
+    from block_quantized_decode_rmsnorm_gb300 import api
+
+    api.copy_stalls(clear=True)
+    case = synth.ffn_case(7)
+    layer = _layer(torch, case)
+    buf = api.FFNBuffers.allocate(HIDDEN, FFN, "cuda")
+    x = to_dev(case["x"], torch)
+    for _ in range(8):
+        api.qg_decode_ffn_q8_0(x, layer, buf, EPS)
+    torch.cuda.synchronize()
+    assert np.all(np.isfinite(x.cpu().numpy()))
+    assert api.copy_stalls() == 0
+    assert api.copy_stalls(clear=True) == 0
+
+
 def test_decode_ffn_out_of_place_host_buffers(torch, orc):
     """The out-of-place layer with its input read from, and its result written to,
     pinned host memory gives the in-place device result bit for bit, eagerly and
