@@ -187,9 +187,9 @@ __host__ __device__ constexpr size_t ffn_up_smem_bytes(int k, bool down = false)
 //    bits 4 and 3), then the warps in shared memory (bits 2, 1, 0), which is the
 //    order of the streaming GEMV's butterfly over 32 lanes: for k <= 1024, h has
 //    the bits that rmsnorm_quantize -> qgemv_q8_0(SiLU) gives.
-// After the wait there are two CTA barriers: the norm statistic's (which also
-// checks the staged slab) and the row partials'; warp 0 then forms h = SiLU(g) u
-// and its Q8_0 block.
+// Before the wait one CTA barrier publishes the landed slab and its f32 scales;
+// after it there are two: the norm statistic's and the row partials'; warp 0
+// then forms h = SiLU(g) u and its Q8_0 block.
 template <int NBL, bool DOWN, bool ROT = false>
 __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
 {
@@ -382,7 +382,7 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
 #pragma unroll
     for (int s = 0; s < 8; ++s) xw.v[s] = __shfl_sync(0xffffffffu, xc, src + s);
     const float xs = __shfl_sync(0xffffffffu, xdf, src);
-    // all sixteen 16-byte reads of the eight rows are issued before the first dot
+    // the eight rows' blocks, then their dots
     float part[8];
     if (DOWN && live) {
         // (the one-launch layer keeps no f32 copy of the scales: shared memory)
