@@ -203,7 +203,6 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_q8_0_reg_kernel(const GemvP
 // registers, so many more warps (and weight bytes) are in flight than in the
 // register-tile kernel at the same batch.
 constexpr int MMA_ROWS = 16;
-constexpr int MMA_GROUP = 8;  // blocks of weights requested together per thread
 
 __device__ __forceinline__ uint2 ld_stream_8B(const void *p)
 {
@@ -221,6 +220,12 @@ __device__ __forceinline__ void mma_s8_16832(int (&c)[4], uint32_t a0, uint32_t 
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// G blocks of weights are requested together per thread (G a multiple of 8 that
+// divides the row's block count): 16 keeps 8 KB a warp in flight with 90
+// registers (five CTAs, 20 warps an SM), against 4 KB and 28 warps for 8, and
+// runs the 262144 x 1024 output head at batch 2-8 in 48.5-49.7 instead of
+// 52.4-53.0 us.
+template <int G>
 __global__ void __launch_bounds__(GEMV_THREADS) gemv_q8_0_mma_kernel(const GemvParams p)
 {
     extern __shared__ __align__(16) uint8_t smem[];
@@ -255,21 +260,29 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_q8_0_mma_kernel(const GemvP
         const int8_t *wA = p.w_qs + rA * K + 8 * t;
         const int8_t *wB = p.w_qs + rB * K + 8 * t;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};  // (row g, batch 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1)
-        for (int j0 = 0; j0 < nb; j0 += MMA_GROUP) {
-            uint2 a[MMA_GROUP], b[MMA_GROUP];
+        for (int j0 = 0; j0 < nb; j0 += G) {
+            uint2 a[G], b[G];
 #pragma unroll
-            for (int u = 0; u < MMA_GROUP; ++u) {
+            for (int u = 0; u < G; ++u) {
                 a[u] = vA ? ld_stream_8B(wA + (j0 + u) * QK) : make_uint2(0u, 0u);
                 b[u] = vB ? ld_stream_8B(wB + (j0 + u) * QK) : make_uint2(0u, 0u);
             }
-            // the eight blocks' scales of rows g and g + 8: 16 bytes each
-            uint4 dA = make_uint4(0u, 0u, 0u, 0u), dB = make_uint4(0u, 0u, 0u, 0u);
-            if (vA) dA = ld_nc_16B(p.w_d + rA * nb + j0);
-            if (vB) dB = ld_nc_16B(p.w_d + rB * nb + j0);
-            const uint16_t *sdA = reinterpret_cast<const uint16_t *>(&dA);
-            const uint16_t *sdB = reinterpret_cast<const uint16_t *>(&dB);
+            // the G blocks' scales of rows g and g + 8, 16 bytes (eight blocks) a load
+            uint4 dA[G / 8], dB[G / 8];
 #pragma unroll
-            for (int u = 0; u < MMA_GROUP; ++u) {
+            for (int q = 0; q < G / 8; ++q) dA[q] = dB[q] = make_uint4(0u, 0u, 0u, 0u);
+            if (vA) {
+#pragma unroll
+                for (int q = 0; q < G / 8; ++q) dA[q] = ld_nc_16B(p.w_d + rA * nb + j0 + 8 * q);
+            }
+            if (vB) {
+#pragma unroll
+                for (int q = 0; q < G / 8; ++q) dB[q] = ld_nc_16B(p.w_d + rB * nb + j0 + 8 * q);
+            }
+            const uint16_t *sdA = reinterpret_cast<const uint16_t *>(dA);
+            const uint16_t *sdB = reinterpret_cast<const uint16_t *>(dB);
+#pragma unroll
+            for (int u = 0; u < G; ++u) {
                 const int blk = j0 + u;
                 const uint2 xf = *reinterpret_cast<const uint2 *>(s_x + g * XS + blk * QK + 8 * t);
                 int c[4] = {0, 0, 0, 0};
@@ -470,14 +483,15 @@ cudaError_t launch_gemv_q8_0(const int8_t *w_qs, const uint16_t *w_d, int64_t n_
     if (batch >= 2 && epi != QG_EPI_SILU_MUL_HALVES && k % 256 == 0 && k <= 4096 &&
         (reinterpret_cast<uintptr_t>(w_d) & 15) == 0) {
         // tensor-core path: 16 rows per warp task, the batch's codes staged in shared memory
-        const void *kern = reinterpret_cast<const void *>(gemv_q8_0_mma_kernel);
+        void (*kernel)(const GemvParams) = p.nb % 16 == 0 ? gemv_q8_0_mma_kernel<16> : gemv_q8_0_mma_kernel<8>;
+        const void *kern = reinterpret_cast<const void *>(kernel);
         const size_t smem = static_cast<size_t>(8) * (k + 32) + static_cast<size_t>(8) * (k / QK) * 4;
         const int occ = max_ctas_per_sm(kern, smem);
         const int wpc = GEMV_THREADS / 32;
         const int64_t need = ((n_rows + MMA_ROWS - 1) / MMA_ROWS + wpc - 1) / wpc;
         const int64_t cap = static_cast<int64_t>(num_sms()) * occ;
-        return launch_pdl(gemv_q8_0_mma_kernel, dim3(static_cast<unsigned>(need < cap ? need : cap)),
-                          dim3(GEMV_THREADS), smem, s, p);
+        return launch_pdl(kernel, dim3(static_cast<unsigned>(need < cap ? need : cap)), dim3(GEMV_THREADS), smem, s,
+                          p);
     }
     if (batch == 1) return dispatch_r<1>(p, nbl, s);
     if (batch == 2) return dispatch_r<2>(p, nbl, s);

@@ -41,6 +41,8 @@ SHAPES = [
     # long-K generic path (K > 4096), batch 1-8 including widths that are padded
     (1, 32, 1), (7, 64, 1), (37, 96, 2), (256, 1024, 1), (1000, 1024, 3), (130, 2080, 1), (64, 3584, 1),
     (50, 4096, 2), (33, 8192, 1), (20, 5120, 5), (300, 1024, 8), (129, 512, 4), (17, 2048, 7), (8, 32, 8),
+    # tensor-core path with 8 blocks a request group (block count not a multiple of 16)
+    (100, 768, 4), (45, 256, 2),
 ]
 
 
