@@ -500,8 +500,9 @@ def config_summary(torch, pk, probe_gbs: float, variants: bool = False) -> tuple
 
 
 def ncu_traffic(kernel_key: str):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, or None when the kernel source changed since it was captured."""
+    """DRAM bytes per launch of a kernel from the committed ncu summary (for
+    "layer_pair", the decode layer's two kernels summed), or None when a kernel
+    source changed since the capture or a record is missing."""
     f = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(f):
         return None
