@@ -319,22 +319,39 @@ __global__ void __launch_bounds__(T2Layout<BN>::THREADS, 1)
             // through shared memory (row stride 40 floats: the 64-bit writes of a
             // half-warp hit distinct banks), so that each store writes 32 columns of a row
             const int64_t m_base = mt * T2_BM + q * 32;
+            const bool rows16 = (p.n & 3) == 0;  // every row of Y starts on 16 bytes
 #pragma unroll
             for (int g = 0; g < NP / 4; ++g) {
+                // the previous group's row copies have read the buffer
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
                 __syncwarp();
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         *reinterpret_cast<float2 *>(xp + (tr + 8 * r) * 40 + 8 * kk + tc) = unpack2(acc[r][4 * g + kk]);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                const bool col_ok = n0 + cbeg + 32 * g + lane < p.n;
+                const int64_t c0 = n0 + cbeg + 32 * g;
+                if (rows16 && c0 + 32 <= p.n) {
+                    // lane r sends row r's 32 values (128 bytes) in one bulk copy
+                    if (m_base + lane < p.m) {
+                        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], 128;" ::"l"(
+                                         p.y + (m_base + lane) * p.n + c0),
+                                     "r"(smem_addr(xp + lane * 40))
+                                     : "memory");
+                    }
+                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                } else {
+                    const bool col_ok = c0 + lane < p.n;
 #pragma unroll 8
-                for (int r = 0; r < 32; ++r) {
-                    const float val = xp[r * 40 + lane];
-                    if (m_base + r < p.m && col_ok) p.y[(m_base + r) * p.n + n0 + cbeg + 32 * g + lane] = val;
+                    for (int r = 0; r < 32; ++r) {
+                        const float val = xp[r * 40 + lane];
+                        if (m_base + r < p.m && col_ok) p.y[(m_base + r) * p.n + c0 + lane] = val;
+                    }
                 }
             }
+            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
         }
     }
 
