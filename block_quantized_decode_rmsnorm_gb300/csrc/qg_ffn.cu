@@ -187,9 +187,10 @@ __host__ __device__ constexpr size_t ffn_up_smem_bytes(int k, bool down = false)
 //    bits 4 and 3), then the warps in shared memory (bits 2, 1, 0), which is the
 //    order of the streaming GEMV's butterfly over 32 lanes: for k <= 1024, h has
 //    the bits that rmsnorm_quantize -> qgemv_q8_0(SiLU) gives.
-// Before the wait one CTA barrier publishes the landed slab and its f32 scales;
-// after it there are two: the norm statistic's and the row partials'; warp 0
-// then forms h = SiLU(g) u and its Q8_0 block.
+// Before the wait one CTA barrier agrees that the slab has landed; after it,
+// while x is loaded, the weight scales are rewritten as f32 in dot order, and
+// two barriers follow: the norm statistic's and the row partials'; warp 0 then
+// forms h = SiLU(g) u and its Q8_0 block.
 template <int NBL, bool DOWN, bool ROT = false>
 __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
 {
@@ -253,24 +254,11 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
         }
     }
 
-    // Still before the wait (the CTA has nothing else to do): once the slab has
-    // landed, the gate|up scales go to f32 in the order the dots read them, so a
-    // lane's eight scales are two 16-byte words and a quarter-warp reads 128
-    // contiguous bytes.  The threads sleep in the barrier unit until then: a spin
-    // here would take issue slots from the kernel whose chain runs on this SM
-    // (measured: 2 us a step).  A copy that has not landed within the limit
-    // leaves NaN outputs for this block.
+    // Still before the wait, the threads see the slab land, asleep in the
+    // barrier unit: a spin here would take issue slots from the kernel whose
+    // chain runs on this SM (measured: 2 us a step).  A copy that has not landed
+    // within the limit leaves NaN outputs for this block.
     const bool ok = mbar_wait_sleep_bounded(&s_bar, 0, kCopyWaitLimitNs);
-    if (!DOWN && ok) {
-        for (int e = t; e < 8 * nb; e += blockDim.x) {
-            const int b = e >> 3, g = e & 7;
-            float f[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) f[i] = h2f(s_wd[(g + 8 * i) * nb + b]);
-            *reinterpret_cast<float4 *>(s_wdf + (2 * b * 8 + g) * 4) = make_float4(f[0], f[1], f[2], f[3]);
-            *reinterpret_cast<float4 *>(s_wdf + ((2 * b + 1) * 8 + g) * 4) = make_float4(f[4], f[5], f[6], f[7]);
-        }
-    }
     const bool staged = __syncthreads_and(ok);
     pdl_wait();
     pdl_trigger();  // the dependent (the layer's down GEMV) only now: see the top of the file
@@ -286,6 +274,19 @@ __global__ void __launch_bounds__(256 * NBL) ffn_up_kernel(const FfnUpParams p)
 
     float4 xv4 = make_float4(0.f, 0.f, 0.f, 0.f);
     if (live) xv4 = *reinterpret_cast<const float4 *>(p.x + xo);
+    // While x is on its way from L2: the gate|up scales to f32 in the order the
+    // dots read them, so a lane's eight scales are two 16-byte words and a
+    // quarter-warp reads 128 contiguous bytes (published by the norm barrier).
+    if (!DOWN && staged) {
+        for (int e = t; e < 8 * nb; e += blockDim.x) {
+            const int b = e >> 3, g = e & 7;
+            float f[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) f[i] = h2f(s_wd[(g + 8 * i) * nb + b]);
+            *reinterpret_cast<float4 *>(s_wdf + (2 * b * 8 + g) * 4) = make_float4(f[0], f[1], f[2], f[3]);
+            *reinterpret_cast<float4 *>(s_wdf + ((2 * b + 1) * 8 + g) * 4) = make_float4(f[4], f[5], f[6], f[7]);
+        }
+    }
     if constexpr (DOWN) {
         // x = r + partials of the previous layer, all loads first, then the sum
         // in partial order (the order qg_decode_layer_finish uses)
