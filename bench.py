@@ -399,9 +399,13 @@ def config_summary(torch, pk, probe_gbs: float, variants: bool = False) -> tuple
         return r, algo, copies
 
     # 1: Q8_0 GEMV 256x1024, and an empty kernel chain of the same launch shape
+    # (the staging GEMV: rows spread over one wave, ceil(256 / SMs) rows and one
+    # warp per row per CTA)
     r, algo, copies = gemv(256, 1024, 1)
     e = hbm_entry(r, algo)
-    gf = capture(torch, lambda: api.qg_measure_launch_chain(copies, 32, 256))
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rpc = -(-256 // sms)
+    gf = capture(torch, lambda: api.qg_measure_launch_chain(copies, -(-256 // rpc), 32 * min(rpc, 8)))
     e["launch_floor_us"] = round(replay_trials(torch, gf, copies)["median"] * 1e6, 3)
     del gf
     cfg["1_gemv_256x1024"] = e
